@@ -1,0 +1,177 @@
+/*
+ * tq.h -- C ABI of the GB300 rotated, bit-packed KV cache (turbo3 / turbo2).
+ *
+ * The method ("llama.cpp に TurboQuant を実装", openalchemy.io): every 128-value K or V
+ * block is stored as one fp16 norm plus one Lloyd-Max code per value of the block
+ * rotated by a 128-point Walsh-Hadamard transform ("What TurboQuant does
+ * differently"); 50 bytes per block for turbo3 (3-bit codes), 34 bytes for turbo2
+ * (2-bit codes) ("How small does it get").  Decode attention reads the packed cache
+ * directly, in the rotated domain ("Current implementation and what's next":
+ * dequantisation fused into the attention kernel, no FP16 K or V materialised).
+ *
+ * Conventions shared by every call:
+ *  - All pointers marked "device" are CUDA device pointers owned by the caller; the
+ *    library never allocates, frees or keeps them.  Pointers marked "host" are
+ *    ordinary host memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Calls that launch work are asynchronous on that stream and never synchronise,
+ *    except tq_device_status.
+ *  - Arguments are validated on the host before anything is launched; a failing
+ *    check returns a status and launches nothing.  No call aborts or throws.
+ *  - Conditions only the GPU can see (a page id outside the pool, a position beyond
+ *    the capacity, a sequence length beyond max_seq_len) skip the offending row and
+ *    record TQ_ERR_OUT_OF_RANGE in a device status word read by tq_device_status.
+ *  - The current CUDA device at the time of the call is the device used.
+ *
+ * Packed block layout (the pages fix the sizes; the bit order is this library's
+ * reading, chosen so that codes turn into table lookups with whole-word shifts):
+ *   bytes [0,2)   norm = fp16(min(|x|, 65504)), little-endian
+ *   bytes [2,34)  8 little-endian u32 words W_0..W_7; value i (w=i/16, j=i%16,
+ *                 r=j/8, k=j%8) has code bits 0,1 at bits 4k+2r, 4k+2r+1 of W_w
+ *   bytes [34,50) turbo3 only: 4 u32 words V_0..V_3; value i (u=i/32, j=i%32,
+ *                 p=j/8, k=j%8) has code bit 2 at bit 4k+p of V_u
+ *
+ * Cache layout (kenji.blog TinyLLaMA article, section 7: preallocate rows for the
+ * maximum context, write the K/V of position N into row N, attend over rows 0..N):
+ *   a packed row holds one token: n_kv_heads x (head_dim/128) blocks, head-major,
+ *   row_bytes = n_kv_heads * head_dim/128 * block_bytes, rows back to back.
+ *   Contiguous cache (page_tokens == 0): row (seq, pos) is at
+ *     base + (seq * capacity_tokens + pos) * row_bytes.
+ *   Paged cache (page_tokens > 0): page = page_table[seq * max_pages_per_seq +
+ *     pos / page_tokens]; row (seq, pos) is at
+ *     base + (page * page_tokens + pos % page_tokens) * row_bytes.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_BLOCK_VALUES 128
+
+/* Symbols of this header are the library's only exported symbols. */
+#if defined(__GNUC__)
+#define TQ_API __attribute__((visibility("default")))
+#else
+#define TQ_API
+#endif
+
+/* Cache types: the code width in bits ("llama.cpp に TurboQuant を実装", intro and
+ * "How to use": turbo3 is the default, turbo2 the experimental 2-bit type). */
+typedef enum tq_type { TQ_TURBO2 = 2, TQ_TURBO3 = 3 } tq_type;
+
+typedef enum tq_status {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad size, bad alignment, bad enum */
+    TQ_ERR_UNSUPPORTED = 2,        /* head_dim not a multiple of 128, shape out of range */
+    TQ_ERR_NOT_INITIALIZED = 3,    /* tq_codebook_init not called for this type/device */
+    TQ_ERR_WORKSPACE_TOO_SMALL = 4,
+    TQ_ERR_CUDA = 5,               /* a CUDA runtime call failed */
+    TQ_ERR_DEVICE_TIMEOUT = 6,     /* a bounded device-side wait gave up */
+    TQ_ERR_OUT_OF_RANGE = 7        /* device saw a page/position/length outside bounds */
+} tq_status;
+
+/* A K or V cache of one layer.  Plain data; the caller fills it and owns `base` and
+ * `page_table`.  K and V are separate caches ("-ctk" / "-ctv": quantised
+ * independently, "How to use"). */
+typedef struct tq_cache {
+    int32_t type;               /* TQ_TURBO3 or TQ_TURBO2 */
+    int32_t n_kv_heads;         /* >= 1 */
+    int32_t head_dim;           /* multiple of 128 ("Numbers on real models") */
+    int32_t page_tokens;        /* 0 = contiguous; else rows per page, multiple of 32 */
+    void *base;                 /* device, 16-byte aligned: the row pool */
+    int64_t capacity_tokens;    /* contiguous: rows reserved per sequence */
+    int32_t n_seqs;             /* sequences addressed by this cache (>= 1) */
+    int32_t max_pages_per_seq;  /* paged: columns of page_table */
+    const int32_t *page_table;  /* paged: device int32 [n_seqs][max_pages_per_seq] */
+    int64_t n_pages;            /* paged: pages in the pool at base */
+} tq_cache;
+
+/* 50 (turbo3) or 34 (turbo2); 0 for an unknown type.  "How small does it get":
+ * 128 values plus one FP16 norm, 0.39 / 0.27 bytes per value. */
+TQ_API size_t tq_block_bytes(int type);
+
+/* Bytes of one packed token row: n_kv_heads * head_dim/128 * tq_block_bytes(type);
+ * 0 if the arguments are invalid. */
+TQ_API size_t tq_row_bytes(int type, int n_kv_heads, int head_dim);
+
+/* Build the type's Lloyd-Max codebook and upload it to `device`.
+ * The codebook is the optimal scalar quantiser for one coordinate of a uniformly
+ * random unit vector in R^128, density (1-y^2)^(125/2) on [-1,1] ("What TurboQuant
+ * does differently": after the rotation every coordinate follows the same law, so a
+ * fixed, data-independent Lloyd-Max codebook is near optimal).  Centroids are solved
+ * in double precision and rounded to fp32; thresholds are the fp32 midpoints.
+ * Idempotent and cheap after the first call; must precede tq_encode / tq_decode /
+ * tq_attn_decode of that type on that device.  Not thread-safe against itself. */
+TQ_API tq_status tq_codebook_init(int type, int device);
+
+/* Host copy of the type's codebook: centroids[2^type] (ascending) and
+ * thresholds[2^type - 1].  Either pointer may be NULL. */
+TQ_API tq_status tq_codebook_get(int type, float *centroids, float *thresholds);
+
+/* Encode n_tokens fp16 token rows into the cache (the per-token write path,
+ * "What TurboQuant does differently": the rotation is cheap enough to live in the
+ * cache-write path).
+ *   src_f16        device fp16 [n_tokens][n_kv_heads][head_dim]; row i starts at
+ *                  src_f16 + i * src_token_stride elements.  16-byte aligned;
+ *                  src_token_stride >= n_kv_heads*head_dim and a multiple of 8.
+ *   seq_ids        device int32 [n_tokens] or NULL (then every token uses seq_id)
+ *   positions      device int32 [n_tokens] or NULL (then token i goes to pos0 + i)
+ * Per block: n = |x| (fixed pairwise fp32 sum, IEEE sqrt), norm = fp16(min(n,65504)),
+ * z = unnormalised FWHT of x, y = z * fl(fl(1/sqrt(128)) / n), code = sign-magnitude
+ * Lloyd-Max index of y.  Codes and norms are bit-identical to the CPU oracle.
+ * n_tokens == 0 is a no-op. */
+TQ_API tq_status tq_encode(const tq_cache *dst, const void *src_f16, int64_t n_tokens,
+                    int64_t src_token_stride, const int32_t *seq_ids,
+                    const int32_t *positions, int32_t seq_id, int64_t pos0,
+                    void *stream);
+
+/* Dequantise rows pos0 .. pos0+n_tokens-1 of sequence seq_id to fp32
+ * dst [n_tokens][n_kv_heads][head_dim] (device): x_hat = norm * W c / sqrt(128)
+ * ("What TurboQuant does differently": the rotation is undone at read time). */
+TQ_API tq_status tq_decode(const tq_cache *src, int32_t seq_id, int64_t pos0, int64_t n_tokens,
+                    float *dst, void *stream);
+
+/* Workspace bytes tq_attn_decode needs for this shape on the current device. */
+TQ_API size_t tq_attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim,
+                               int64_t max_seq_len);
+
+/* Single-token decode attention over the packed caches (kenji.blog article, section
+ * 8: out = softmax(q K^T * scale) V over the cached positions; TinyLLaMA article 4.3:
+ * query head h reads KV head floor(h / (n_q_heads / n_kv_heads))).
+ *   k, v           caches of one layer; same n_kv_heads and head_dim; the types may
+ *                  differ (mixed "-ctk" / "-ctv").  Batch entry s reads cache
+ *                  sequence s.
+ *   q_f16          device fp16 [n_seqs][n_q_heads][head_dim], 16-byte aligned
+ *   seq_lens       device int32 [n_seqs]: attend to positions [0, seq_lens[s]); the
+ *                  caller appends the current token first (decode-step data flow of
+ *                  the kenji.blog article, section 8).  0 gives a zero output.
+ *   max_seq_len    host upper bound of seq_lens (sizes the split-K grid)
+ *   softmax_scale  score scale; pass 0 for 1/sqrt(head_dim)
+ *   out            device fp32 [n_seqs][n_q_heads][head_dim]
+ *   workspace      device scratch of at least tq_attn_workspace_bytes(...) bytes,
+ *                  16-byte aligned; contents need no initialisation
+ * The scores are computed as |k| * (W q / sqrt(128)) . c(codes) and the values
+ * accumulated as sum p |v| c(codes), both in the rotated domain, with one inverse
+ * FWHT per output block; no fp16 K or V is formed. */
+TQ_API tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void *q_f16,
+                         int n_seqs, int n_q_heads, const int32_t *seq_lens,
+                         int64_t max_seq_len, float softmax_scale, float *out,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronise `stream`, then read and clear the device status word of the current
+ * device: *status_out = TQ_OK or the first device-side error recorded since the
+ * last read.  Returns TQ_ERR_CUDA if synchronisation fails. */
+TQ_API tq_status tq_device_status(void *stream, int32_t *status_out);
+
+/* Static, human-readable name of a status code. */
+TQ_API const char *tq_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,112 @@
+"""GB300 rotated, bit-packed KV cache (turbo3 / turbo2) -- Python binding.
+
+Thin marshalling layer over the C ABI of libtq.so (include/tq.h).  PyTorch supplies
+device memory and streams; every step of encode, decode and attention runs in the
+library's sm_103a kernels.  There is no CPU fallback: calls raise if the library is
+missing.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._lib import (TQ_BLOCK_VALUES, TQ_TURBO2, TQ_TURBO3, TQError, TqCache, check, load)
+
+__all__ = ["TQ_TURBO2", "TQ_TURBO3", "TQ_BLOCK_VALUES", "TQError", "TqCache", "KVCache",
+           "block_bytes", "row_bytes", "codebook_init", "codebook_get", "encode", "decode",
+           "attn_workspace_bytes", "attn_decode", "device_status", "load"]
+
+
+def _stream_ptr(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def block_bytes(tq_type: int) -> int:
+    return int(load().tq_block_bytes(tq_type))
+
+
+def row_bytes(tq_type: int, n_kv_heads: int, head_dim: int) -> int:
+    return int(load().tq_row_bytes(tq_type, n_kv_heads, head_dim))
+
+
+def codebook_init(tq_type: int, device: int = 0):
+    check(load().tq_codebook_init(tq_type, device), "tq_codebook_init")
+
+
+def codebook_get(tq_type: int):
+    import numpy as np
+    levels = 1 << tq_type
+    c = np.zeros(levels, np.float32)
+    t = np.zeros(levels - 1, np.float32)
+    check(load().tq_codebook_get(tq_type, c.ctypes.data_as(ctypes.c_void_p),
+                                 t.ctypes.data_as(ctypes.c_void_p)), "tq_codebook_get")
+    return c, t
+
+
+class KVCache:
+    """One layer's K or V cache: a PyTorch uint8 device buffer plus its tq_cache view.
+
+    Contiguous: ``capacity_tokens`` rows per sequence.  Paged: pass ``page_tokens`` and an
+    int32 device ``page_table`` [n_seqs, max_pages]; the pool holds ``n_pages`` pages.
+    """
+
+    def __init__(self, tq_type: int, n_kv_heads: int, head_dim: int, *, n_seqs: int = 1,
+                 capacity_tokens: int = 0, page_tokens: int = 0, page_table=None,
+                 n_pages: int = 0, device=None, buffer=None):
+        import torch
+        self.type, self.n_kv_heads, self.head_dim = tq_type, n_kv_heads, head_dim
+        self.row_bytes = row_bytes(tq_type, n_kv_heads, head_dim)
+        if self.row_bytes == 0:
+            raise TQError(1, "KVCache: bad shape")
+        rows = n_pages * page_tokens if page_tokens else n_seqs * capacity_tokens
+        if buffer is None:
+            buffer = torch.zeros(rows * self.row_bytes, dtype=torch.uint8,
+                                 device=device if device is not None else "cuda")
+        self.buffer = buffer
+        self.page_table = page_table
+        self.view = TqCache(tq_type, n_kv_heads, head_dim, page_tokens, buffer.data_ptr(),
+                            capacity_tokens, n_seqs, page_table.shape[1] if page_table is not None else 0,
+                            page_table.data_ptr() if page_table is not None else None, n_pages)
+
+    @property
+    def nbytes(self) -> int:
+        return self.buffer.numel()
+
+
+def encode(cache: KVCache, src, *, seq_ids=None, positions=None, seq_id: int = 0, pos0: int = 0,
+           stream=None):
+    """src: fp16 device tensor [n_tokens, n_kv_heads*head_dim] (row stride = src.stride(0))."""
+    n = src.shape[0]
+    stride = src.stride(0) if src.dim() > 1 else cache.n_kv_heads * cache.head_dim
+    check(load().tq_encode(ctypes.byref(cache.view), _ptr(src), n, stride, _ptr(seq_ids),
+                           _ptr(positions), seq_id, pos0, _stream_ptr(stream)), "tq_encode")
+
+
+def decode(cache: KVCache, seq_id: int, pos0: int, n_tokens: int, out, stream=None):
+    check(load().tq_decode(ctypes.byref(cache.view), seq_id, pos0, n_tokens, _ptr(out),
+                           _stream_ptr(stream)), "tq_decode")
+
+
+def attn_workspace_bytes(n_seqs: int, n_q_heads: int, head_dim: int, max_seq_len: int) -> int:
+    return int(load().tq_attn_workspace_bytes(n_seqs, n_q_heads, head_dim, max_seq_len))
+
+
+def attn_decode(k: KVCache, v: KVCache, q, seq_lens, max_seq_len: int, out, workspace,
+                softmax_scale: float = 0.0, stream=None):
+    """q: fp16 [n_seqs, n_q_heads, head_dim]; seq_lens int32 [n_seqs]; out fp32 like q."""
+    n_seqs, n_q_heads = q.shape[0], q.shape[1]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(load().tq_attn_decode(ctypes.byref(k.view), ctypes.byref(v.view), _ptr(q), n_seqs,
+                                n_q_heads, _ptr(seq_lens), max_seq_len, softmax_scale, _ptr(out),
+                                _ptr(workspace), ws_bytes, _stream_ptr(stream)), "tq_attn_decode")
+
+
+def device_status(stream=None) -> int:
+    st = ctypes.c_int32(0)
+    check(load().tq_device_status(_stream_ptr(stream), ctypes.byref(st)), "tq_device_status")
+    return int(st.value)

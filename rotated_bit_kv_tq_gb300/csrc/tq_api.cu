@@ -1,0 +1,225 @@
+// tq_api.cu -- the C ABI: host-side validation, codebook set-up, status word.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "tq_internal.cuh"
+
+namespace tq {
+
+__device__ int32_t g_status = 0;
+__constant__ Codebook c_codebook[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+bool g_ready[kMaxDevices][2];
+Codebook g_host_cb[2];
+bool g_host_cb_done[2];
+std::mutex g_mu;
+
+bool valid_type(int type) { return type == TQ_TURBO2 || type == TQ_TURBO3; }
+
+const Codebook &host_codebook(int type) {
+    int i = cb_index(type);
+    if (!g_host_cb_done[i]) {
+        const int levels = 1 << type;
+        double c[8];
+        solve_codebook(levels, c);
+        Codebook cb;
+        std::memset(&cb, 0, sizeof cb);
+        for (int j = 0; j < levels; ++j) {
+            cb.centroid[j] = (float)c[j];
+            cb.centroid_h[j] = __float2half_rn(cb.centroid[j]);
+        }
+        // fp32 midpoints of the fp32 centroids
+        for (int j = 0; j + 1 < levels; ++j)
+            cb.threshold[j] = (cb.centroid[j] + cb.centroid[j + 1]) * 0.5f;
+        g_host_cb[i] = cb;
+        g_host_cb_done[i] = true;
+    }
+    return g_host_cb[i];
+}
+
+}  // namespace
+
+bool codebook_ready(int type, int device) {
+    if (device < 0 || device >= kMaxDevices || !valid_type(type)) return false;
+    return g_ready[device][cb_index(type)];
+}
+
+tq_status check_cuda(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 1;
+    return n;
+}
+
+CacheView make_view(const tq_cache &c) {
+    CacheView v;
+    v.base = static_cast<uint8_t *>(c.base);
+    v.page_table = c.page_table;
+    v.capacity = c.capacity_tokens;
+    v.n_pages = c.n_pages;
+    v.page_tokens = c.page_tokens;
+    v.max_pages = c.max_pages_per_seq;
+    v.n_seqs = c.n_seqs;
+    v.row_bytes = (int32_t)tq_row_bytes(c.type, c.n_kv_heads, c.head_dim);
+    return v;
+}
+
+tq_status validate_cache(const tq_cache *c) {
+    if (!c || !c->base) return TQ_ERR_INVALID_ARGUMENT;
+    if (!valid_type(c->type)) return TQ_ERR_INVALID_ARGUMENT;
+    if (c->n_kv_heads < 1 || c->head_dim < 1 || c->n_seqs < 1) return TQ_ERR_INVALID_ARGUMENT;
+    if (c->head_dim % kBlock != 0) return TQ_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(c->base) % 16 != 0) return TQ_ERR_INVALID_ARGUMENT;
+    if ((int64_t)c->n_kv_heads * (c->head_dim / kBlock) > 128) return TQ_ERR_UNSUPPORTED;
+    if (c->page_tokens < 0) return TQ_ERR_INVALID_ARGUMENT;
+    if (c->page_tokens == 0) {
+        if (c->capacity_tokens < 1) return TQ_ERR_INVALID_ARGUMENT;
+    } else {
+        if (c->page_tokens % 32 != 0) return TQ_ERR_UNSUPPORTED;
+        if (!c->page_table || c->max_pages_per_seq < 1 || c->n_pages < 1)
+            return TQ_ERR_INVALID_ARGUMENT;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    if (!codebook_ready(c->type, dev)) return TQ_ERR_NOT_INITIALIZED;
+    return TQ_OK;
+}
+
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+size_t tq_block_bytes(int type) { return valid_type(type) ? (size_t)block_bytes(type) : 0; }
+
+size_t tq_row_bytes(int type, int n_kv_heads, int head_dim) {
+    if (!valid_type(type) || n_kv_heads < 1 || head_dim < kBlock || head_dim % kBlock) return 0;
+    return (size_t)n_kv_heads * (size_t)(head_dim / kBlock) * (size_t)block_bytes(type);
+}
+
+tq_status tq_codebook_get(int type, float *centroids, float *thresholds) {
+    if (!valid_type(type)) return TQ_ERR_INVALID_ARGUMENT;
+    std::lock_guard<std::mutex> lock(g_mu);
+    const Codebook &cb = host_codebook(type);
+    const int levels = 1 << type;
+    if (centroids) std::memcpy(centroids, cb.centroid, sizeof(float) * levels);
+    if (thresholds) std::memcpy(thresholds, cb.threshold, sizeof(float) * (levels - 1));
+    return TQ_OK;
+}
+
+tq_status tq_codebook_init(int type, int device) {
+    if (!valid_type(type) || device < 0 || device >= kMaxDevices) return TQ_ERR_INVALID_ARGUMENT;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_ready[device][cb_index(type)]) return TQ_OK;
+    const Codebook &cb = host_codebook(type);
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaSetDevice(device) != cudaSuccess) return TQ_ERR_CUDA;
+    cudaError_t e = cudaMemcpyToSymbol(c_codebook, &cb, sizeof(Codebook),
+                                       sizeof(Codebook) * cb_index(type));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    cudaSetDevice(prev);
+    if (e != cudaSuccess) return TQ_ERR_CUDA;
+    g_ready[device][cb_index(type)] = true;
+    return TQ_OK;
+}
+
+tq_status tq_encode(const tq_cache *dst, const void *src_f16, int64_t n_tokens,
+                    int64_t src_token_stride, const int32_t *seq_ids, const int32_t *positions,
+                    int32_t seq_id, int64_t pos0, void *stream) {
+    tq_status st = validate_cache(dst);
+    if (st != TQ_OK) return st;
+    if (n_tokens < 0) return TQ_ERR_INVALID_ARGUMENT;
+    if (n_tokens == 0) return TQ_OK;
+    if (!src_f16 || reinterpret_cast<uintptr_t>(src_f16) % 16) return TQ_ERR_INVALID_ARGUMENT;
+    const int64_t row_elems = (int64_t)dst->n_kv_heads * dst->head_dim;
+    if (src_token_stride < row_elems || src_token_stride % 8) return TQ_ERR_INVALID_ARGUMENT;
+    if (!positions && pos0 < 0) return TQ_ERR_INVALID_ARGUMENT;
+    if (!seq_ids && (seq_id < 0 || seq_id >= dst->n_seqs)) return TQ_ERR_INVALID_ARGUMENT;
+    if (n_tokens > (int64_t)1 << 40) return TQ_ERR_UNSUPPORTED;
+    return launch_encode(*dst, src_f16, n_tokens, src_token_stride, seq_ids, positions, seq_id,
+                         pos0, static_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_decode(const tq_cache *src, int32_t seq_id, int64_t pos0, int64_t n_tokens,
+                    float *dst, void *stream) {
+    tq_status st = validate_cache(src);
+    if (st != TQ_OK) return st;
+    if (n_tokens < 0 || pos0 < 0 || seq_id < 0 || seq_id >= src->n_seqs)
+        return TQ_ERR_INVALID_ARGUMENT;
+    if (n_tokens == 0) return TQ_OK;
+    if (!dst || reinterpret_cast<uintptr_t>(dst) % 16) return TQ_ERR_INVALID_ARGUMENT;
+    return launch_decode(*src, seq_id, pos0, n_tokens, dst, static_cast<cudaStream_t>(stream));
+}
+
+size_t tq_attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max_seq_len) {
+    if (n_seqs < 1 || n_q_heads < 1 || head_dim < kBlock || head_dim % kBlock || max_seq_len < 0)
+        return 0;
+    return attn_workspace_bytes(n_seqs, n_q_heads, head_dim, max_seq_len, device_sm_count());
+}
+
+tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void *q_f16, int n_seqs,
+                         int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
+                         float softmax_scale, float *out, void *workspace, size_t ws_bytes,
+                         void *stream) {
+    tq_status st = validate_cache(k);
+    if (st != TQ_OK) return st;
+    st = validate_cache(v);
+    if (st != TQ_OK) return st;
+    if (k->n_kv_heads != v->n_kv_heads || k->head_dim != v->head_dim)
+        return TQ_ERR_INVALID_ARGUMENT;
+    if (n_seqs < 1 || n_seqs > k->n_seqs || n_seqs > v->n_seqs) return TQ_ERR_INVALID_ARGUMENT;
+    if (n_q_heads < 1 || n_q_heads % k->n_kv_heads) return TQ_ERR_INVALID_ARGUMENT;
+    if (n_q_heads / k->n_kv_heads > 16 || n_q_heads > 128) return TQ_ERR_UNSUPPORTED;
+    if (max_seq_len < 0 || max_seq_len > ((int64_t)1 << 31) - 1) return TQ_ERR_INVALID_ARGUMENT;
+    if (!q_f16 || !seq_lens || !out) return TQ_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(q_f16) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+        return TQ_ERR_INVALID_ARGUMENT;
+    if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale)) return TQ_ERR_INVALID_ARGUMENT;
+    if (softmax_scale == 0.0f) softmax_scale = 1.0f / std::sqrt((float)k->head_dim);
+    size_t need = tq_attn_workspace_bytes(n_seqs, n_q_heads, k->head_dim, max_seq_len);
+    if (need > 0 && (!workspace || ws_bytes < need)) return TQ_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16) return TQ_ERR_INVALID_ARGUMENT;
+    return launch_attn(*k, *v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len, softmax_scale,
+                       out, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_device_status(void *stream, int32_t *status_out) {
+    if (!status_out) return TQ_ERR_INVALID_ARGUMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t host = 0, zero = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaMemcpyFromSymbolAsync(&host, g_status, sizeof host, 0, cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return TQ_ERR_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return TQ_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TQ_ERR_CUDA;
+    *status_out = host;
+    return TQ_OK;
+}
+
+const char *tq_status_str(int status) {
+    switch (status) {
+        case TQ_OK: return "TQ_OK";
+        case TQ_ERR_INVALID_ARGUMENT: return "TQ_ERR_INVALID_ARGUMENT";
+        case TQ_ERR_UNSUPPORTED: return "TQ_ERR_UNSUPPORTED";
+        case TQ_ERR_NOT_INITIALIZED: return "TQ_ERR_NOT_INITIALIZED";
+        case TQ_ERR_WORKSPACE_TOO_SMALL: return "TQ_ERR_WORKSPACE_TOO_SMALL";
+        case TQ_ERR_CUDA: return "TQ_ERR_CUDA";
+        case TQ_ERR_DEVICE_TIMEOUT: return "TQ_ERR_DEVICE_TIMEOUT";
+        case TQ_ERR_OUT_OF_RANGE: return "TQ_ERR_OUT_OF_RANGE";
+        default: return "TQ_UNKNOWN_STATUS";
+    }
+}
+
+}  // extern "C"

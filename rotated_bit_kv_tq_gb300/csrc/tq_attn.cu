@@ -1,0 +1,422 @@
+// tq_attn.cu -- fused single-token decode attention over the packed cache
+// (CUDA-core, fp32 arithmetic).
+//
+// kenji.blog inference-engine article, section 8: out = softmax(q K^T / sqrt(d)) V over
+// the cached positions; TinyLLaMA article 4.3: query head h reads KV head floor(h / G).
+// "llama.cpp に TurboQuant を実装", "Current implementation and what's next": the
+// dequantisation is fused into the attention kernel so that no FP16 key or value is
+// materialised.  Because W/sqrt(128) is orthonormal and symmetric,
+//     q . k_hat = |k| (W q / sqrt(128)) . c(codes_k)
+//     sum_t p_t v_hat_t = (1/sqrt(128)) W sum_t p_t |v_t| c(codes_v)
+// so q is rotated once per call, scores and the value sum run in the rotated domain,
+// and one inverse FWHT per output block finishes the job.
+//
+// Split-K: the context of every sequence is cut into equal token ranges, one CTA per
+// (range, sequence).  Each CTA streams its packed K/V rows through shared memory in
+// tiles, keeps an online softmax (running max m, sum l) and a rotated-domain value
+// accumulator per query head, and writes (acc, m, l) to the workspace.  A second kernel
+// merges the ranges with the usual log-sum-exp rescaling and applies the inverse FWHT.
+#include <cmath>
+
+#include "tq_internal.cuh"
+#include "tq_simd.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTokenAlign = 32;       // split ranges start on multiples of this
+constexpr int kMaxG = 8;              // query heads per KV head handled in registers
+constexpr int kMaxNb = 2;             // 128-blocks per head handled in registers
+constexpr int kTileBudget = 96 * 1024;  // shared bytes for one K+V tile
+
+struct AttnParams {
+    CacheView kc, vc;
+    const __half *q;
+    const int32_t *seq_lens;
+    float *part;   // [n_seqs][n_splits][Hq][D + 2]
+    float *out;    // [n_seqs][Hq][D]
+    float scale;   // softmax scale (1/sqrt(D) by default)
+    int64_t max_len;
+    int32_t n_q_heads, n_kv_heads, group, head_dim, nb;
+    int32_t n_splits, tokens_per_split, tile_tokens;
+};
+
+struct SplitPlan {
+    int n_splits;
+    int tokens_per_split;
+};
+
+SplitPlan plan_splits(int n_seqs, int64_t max_len, int sm_count) {
+    SplitPlan pl;
+    const int64_t target = max64(1, (2LL * sm_count + n_seqs - 1) / n_seqs);
+    int64_t tps = (max64(max_len, 1) + target - 1) / target;
+    tps = (tps + kTokenAlign - 1) / kTokenAlign * kTokenAlign;
+    if (tps < kTokenAlign) tps = kTokenAlign;
+    pl.tokens_per_split = (int)tps;
+    pl.n_splits = (int)max64(1, (max_len + tps - 1) / tps);
+    return pl;
+}
+
+// Rotate the query of one (head, block) pair held by a warp, four values per lane:
+// returns the lane's four values of W q_b (canonical butterfly order).
+__device__ __forceinline__ void warp_fwht4(float v[4], int lane) {
+    float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2;
+    v[1] = a1 + a3;
+    v[2] = a0 - a2;
+    v[3] = a1 - a3;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = lane & m;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
+            v[e] = upper ? o - v[e] : v[e] + o;
+        }
+    }
+}
+
+// Code of value i of a packed block (layout of tq.h).
+template <int TYPE>
+__device__ __forceinline__ int code_of(const uint8_t *b, int i) {
+    const int j = i & 15;
+    const int lb = 32 * (i >> 4) + 4 * (j & 7) + 2 * (j >> 3);
+    int code = (b[2 + (lb >> 3)] >> (lb & 7)) & 3;
+    if (TYPE == TQ_TURBO3) {
+        const int jv = i & 31;
+        const int hb = 32 * (i >> 5) + 4 * (jv & 7) + (jv >> 3);
+        code |= ((b[34 + (hb >> 3)] >> (hb & 7)) & 1) << 2;
+    }
+    return code;
+}
+
+__device__ __forceinline__ float norm_of(const uint8_t *b) {
+    return __half2float(__ushort_as_half((uint16_t)(b[0] | (b[1] << 8))));
+}
+
+// Copy `bytes` bytes of one packed row (2-byte aligned, 16-byte when possible) into smem.
+__device__ __forceinline__ void copy_row(uint8_t *dst, const uint8_t *src, int bytes, int lane) {
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && (bytes & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        for (int c = lane; c < bytes / 16; c += 32)
+            reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
+    } else {
+        for (int c = lane; c < bytes / 2; c += 32)
+            reinterpret_cast<uint16_t *>(dst)[c] = reinterpret_cast<const uint16_t *>(src)[c];
+    }
+}
+
+template <int TK, int TV>
+__global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int Hq = p.n_q_heads, D = p.head_dim, G = p.group, Hkv = p.n_kv_heads;
+    const int TT = p.tile_tokens;
+    const int Rk = p.kc.row_bytes, Rv = p.vc.row_bytes;
+    const int Rk16 = (Rk + 15) & ~15, Rv16 = (Rv + 15) & ~15;
+    float *qs = reinterpret_cast<float *>(smem);                 // [Hq][D]
+    float *S = qs + Hq * D;                                      // [Hq][TT]
+    float *m_run = S + Hq * TT;                                  // [Hq]
+    float *l_run = m_run + Hq;                                   // [Hq]
+    float *alpha = l_run + Hq;                                   // [Hq]
+    float *ck = alpha + Hq;                                      // [8]
+    float *cv = ck + 8;                                          // [8]
+    uint8_t *kt = reinterpret_cast<uint8_t *>(cv + 8);           // [TT][Rk16]
+    kt = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(kt) + 15) & ~uintptr_t(15));
+    uint8_t *vt = kt + TT * Rk16;                                // [TT][Rv16]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int seq = blockIdx.y, split = blockIdx.x;
+    int64_t len = p.seq_lens[seq];
+    if (len < 0 || len > p.max_len) {
+        if (tid == 0) record_error(TQ_ERR_OUT_OF_RANGE);
+        len = len < 0 ? 0 : p.max_len;
+    }
+    const int64_t t_begin = (int64_t)split * p.tokens_per_split;
+    const int64_t t_end = min64(len, t_begin + p.tokens_per_split);
+
+    if (tid < 8) {
+        ck[tid] = tid < (1 << TK) ? c_codebook[cb_index(TK)].centroid[tid] : 0.f;
+        cv[tid] = tid < (1 << TV) ? c_codebook[cb_index(TV)].centroid[tid] : 0.f;
+    }
+    for (int h = tid; h < Hq; h += kThreads) {
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.f;
+    }
+    // ---- rotate q once: qs = W q_b * (scale / sqrt(128)) per (head, block)
+    const float qscale = p.scale * kInvSqrt128;
+    for (int hb = warp; hb < Hq * p.nb; hb += kWarps) {
+        const int h = hb / p.nb, b = hb - h * p.nb;
+        const __half *qp = p.q + ((int64_t)seq * Hq + h) * D + b * kBlock + 4 * lane;
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = __half2float(qp[e]);
+        warp_fwht4(v, lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qs[h * D + b * kBlock + 4 * lane + e] = v[e] * qscale;
+    }
+
+    // V accumulators: warp w owns KV heads g = w, w + 8, ...; lane owns values
+    // 4*lane .. 4*lane+3 of every block.  acc[h_local * nb + b][e].
+    float acc[kMaxG][kMaxNb][4];
+
+    for (int g0 = 0; g0 < Hkv; g0 += kWarps) {
+        const int g = g0 + warp;  // this warp's KV head in this pass
+#pragma unroll
+        for (int a = 0; a < kMaxG; ++a)
+#pragma unroll
+            for (int b = 0; b < kMaxNb; ++b)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[a][b][e] = 0.f;
+        // (heads of other passes keep running statistics in m_run / l_run, but the
+        //  accumulators are per pass, so passes re-stream the tiles: Hkv <= 8 is one pass)
+        __syncthreads();
+        for (int64_t t0 = t_begin; t0 < t_end; t0 += TT) {
+            const int nt = (int)min64(TT, t_end - t0);
+            // ---- stage K and V rows
+            for (int r = warp; r < nt; r += kWarps) {
+                const uint8_t *krow = row_ptr(p.kc, seq, t0 + r);
+                const uint8_t *vrow = row_ptr(p.vc, seq, t0 + r);
+                if (krow) copy_row(kt + r * Rk16, krow, Rk, lane);
+                if (vrow) copy_row(vt + r * Rv16, vrow, Rv, lane);
+            }
+            __syncthreads();
+            // ---- scores: thread <-> (KV head gg, token t); only this pass's heads
+            const int gpass = min(kWarps, Hkv - g0);
+            for (int pi = tid; pi < gpass * TT; pi += kThreads) {
+                const int gg = g0 + pi / TT, t = pi % TT;
+                float sc[kMaxG];
+#pragma unroll
+                for (int h = 0; h < kMaxG; ++h) sc[h] = 0.f;
+                if (t < nt) {
+                    for (int b = 0; b < p.nb; ++b) {
+                        const uint8_t *blk = kt + t * Rk16 + (gg * p.nb + b) * block_bytes(TK);
+                        float dot[kMaxG];
+#pragma unroll
+                        for (int h = 0; h < kMaxG; ++h) dot[h] = 0.f;
+                        const float *qb = qs + (gg * G) * D + b * kBlock;
+                        for (int i = 0; i < kBlock; ++i) {
+                            const float c = ck[code_of<TK>(blk, i)];
+#pragma unroll
+                            for (int h = 0; h < kMaxG; ++h)
+                                if (h < G) dot[h] = fmaf(c, qb[h * D + i], dot[h]);
+                        }
+                        const float n = norm_of(blk);
+#pragma unroll
+                        for (int h = 0; h < kMaxG; ++h) sc[h] = fmaf(n, dot[h], sc[h]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < kMaxG; ++h)
+                    if (h < G) S[(gg * G + h) * TT + t] = t < nt ? sc[h] : -INFINITY;
+            }
+            __syncthreads();
+            // ---- online softmax, warp per query head of this pass
+            for (int hh = warp; hh < gpass * G; hh += kWarps) {
+                const int h = g0 * G + hh;
+                float mx = -INFINITY;
+                for (int t = lane; t < TT; t += 32) mx = fmaxf(mx, S[h * TT + t]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float m_old = m_run[h];
+                const float m_new = fmaxf(m_old, mx);
+                float sum = 0.f;
+                for (int t = lane; t < TT; t += 32) {
+                    const float s = S[h * TT + t];
+                    const float pr = (s == -INFINITY) ? 0.f : __expf(s - m_new);
+                    S[h * TT + t] = pr;
+                    sum += pr;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                __syncwarp();
+                if (lane == 0) {
+                    const float al = (m_old == -INFINITY) ? 0.f : __expf(m_old - m_new);
+                    alpha[h] = al;
+                    m_run[h] = m_new;
+                    l_run[h] = l_run[h] * al + sum;
+                }
+            }
+            __syncthreads();
+            // ---- rotated-domain value accumulation
+            if (g < Hkv) {
+#pragma unroll
+                for (int hl = 0; hl < kMaxG; ++hl) {
+                    if (hl < G) {
+                        const float al = alpha[g * G + hl];
+#pragma unroll
+                        for (int b = 0; b < kMaxNb; ++b)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[hl][b][e] *= al;
+                    }
+                }
+                for (int t = 0; t < nt; ++t) {
+#pragma unroll
+                    for (int b = 0; b < kMaxNb; ++b) {
+                        if (b >= p.nb) break;
+                        const uint8_t *blk = vt + t * Rv16 + (g * p.nb + b) * block_bytes(TV);
+                        const float n = norm_of(blk);
+                        float c[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) c[e] = cv[code_of<TV>(blk, 4 * lane + e)];
+#pragma unroll
+                        for (int hl = 0; hl < kMaxG; ++hl) {
+                            if (hl < G) {
+                                const float w = S[(g * G + hl) * TT + t] * n;
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) acc[hl][b][e] = fmaf(w, c[e], acc[hl][b][e]);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        // ---- write this pass's partials
+        if (g < Hkv) {
+#pragma unroll
+            for (int hl = 0; hl < kMaxG; ++hl) {
+                if (hl >= G) break;
+                const int h = g * G + hl;
+                float *dst = p.part + (((int64_t)seq * p.n_splits + split) * Hq + h) * (D + 2);
+#pragma unroll
+                for (int b = 0; b < kMaxNb; ++b) {
+                    if (b >= p.nb) break;
+                    float *d = dst + b * kBlock + 4 * lane;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) d[e] = acc[hl][b][e];
+                }
+                if (lane == 0) {
+                    dst[D] = m_run[h];
+                    dst[D + 1] = l_run[h];
+                }
+            }
+        }
+    }
+}
+
+// Merge the split partials of one (sequence, head) and undo the rotation.
+__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
+    extern __shared__ __align__(16) float msm[];   // [D] output + [n_splits] weights
+    const int h = blockIdx.x, seq = blockIdx.y, D = p.head_dim, tid = threadIdx.x;
+    float *o = msm;
+    float *wts = msm + D;
+    const float *base = p.part + ((int64_t)seq * p.n_splits * p.n_q_heads + h) * (D + 2);
+    const int64_t sstride = (int64_t)p.n_q_heads * (D + 2);
+    // global max and weights
+    __shared__ float red[32];
+    float mx = -INFINITY;
+    for (int s = tid; s < p.n_splits; s += blockDim.x) mx = fmaxf(mx, base[s * sstride + D]);
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((tid & 31) == 0) red[tid >> 5] = mx;
+    __syncthreads();
+    mx = -INFINITY;
+    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) mx = fmaxf(mx, red[w]);
+    __syncthreads();
+    float lsum = 0.f;
+    for (int s = tid; s < p.n_splits; s += blockDim.x) {
+        const float m = base[s * sstride + D];
+        const float w = (m == -INFINITY) ? 0.f : __expf(m - mx);
+        wts[s] = w;
+        lsum += w * base[s * sstride + D + 1];
+    }
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    if ((tid & 31) == 0) red[tid >> 5] = lsum;
+    __syncthreads();
+    lsum = 0.f;
+    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) lsum += red[w];
+    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+    for (int i = tid; i < D; i += blockDim.x) {
+        float a = 0.f;
+        for (int s = 0; s < p.n_splits; ++s) {
+            const float w = wts[s];
+            if (w != 0.f) a = fmaf(w, base[s * sstride + i], a);
+        }
+        o[i] = a * inv;
+    }
+    __syncthreads();
+    // inverse rotation per 128-block: (1/sqrt(128)) W o_b
+    for (int hlen = 1; hlen < kBlock; hlen <<= 1) {
+        for (int i = tid; i < D; i += blockDim.x) {
+            const int ib = i & (kBlock - 1);
+            if (!(ib & hlen)) {
+                const float a = o[i], b = o[i + hlen];
+                o[i] = a + b;
+                o[i + hlen] = a - b;
+            }
+        }
+        __syncthreads();
+    }
+    float *dst = p.out + ((int64_t)seq * p.n_q_heads + h) * D;
+    for (int i = tid; i < D; i += blockDim.x) dst[i] = o[i] * kInvSqrt128;
+}
+
+size_t partial_smem(const AttnParams &p) {
+    const int Rk16 = (p.kc.row_bytes + 15) & ~15, Rv16 = (p.vc.row_bytes + 15) & ~15;
+    return sizeof(float) * ((size_t)p.n_q_heads * p.head_dim + (size_t)p.n_q_heads * p.tile_tokens +
+                            3 * (size_t)p.n_q_heads + 16) +
+           16 + (size_t)p.tile_tokens * (Rk16 + Rv16);
+}
+
+template <int TK, int TV>
+tq_status launch_attn_t(const AttnParams &p, int n_seqs, cudaStream_t stream) {
+    const size_t smem = partial_smem(p);
+    if (smem > 220 * 1024) return TQ_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(attn_partial_kernel<TK, TV>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    attn_partial_kernel<TK, TV><<<dim3(p.n_splits, n_seqs), kThreads, smem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
+    const size_t msmem = sizeof(float) * ((size_t)p.head_dim + (size_t)p.n_splits);
+    if (msmem > 48 * 1024 &&
+        cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)msmem) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    attn_merge_kernel<<<dim3(p.n_q_heads, n_seqs), min(256, p.head_dim), msmem, stream>>>(p);
+    return check_cuda(cudaGetLastError());
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max_seq_len,
+                            int sm_count) {
+    const SplitPlan pl = plan_splits(n_seqs, max_seq_len, sm_count);
+    return sizeof(float) * (size_t)n_seqs * pl.n_splits * n_q_heads * (head_dim + 2);
+}
+
+tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
+                      int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
+                      float *out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    AttnParams p;
+    p.kc = make_view(k);
+    p.vc = make_view(v);
+    p.q = static_cast<const __half *>(q);
+    p.seq_lens = seq_lens;
+    p.part = static_cast<float *>(ws);
+    p.out = out;
+    p.scale = scale;
+    p.max_len = max_seq_len;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = k.n_kv_heads;
+    p.group = n_q_heads / k.n_kv_heads;
+    p.head_dim = k.head_dim;
+    p.nb = k.head_dim / kBlock;
+    if (p.group > kMaxG || p.nb > kMaxNb) return TQ_ERR_UNSUPPORTED;
+    if ((size_t)n_q_heads * k.head_dim > 16384) return TQ_ERR_UNSUPPORTED;
+    const SplitPlan pl = plan_splits(n_seqs, max_seq_len, device_sm_count());
+    p.n_splits = pl.n_splits;
+    p.tokens_per_split = pl.tokens_per_split;
+    const int Rk16 = (p.kc.row_bytes + 15) & ~15, Rv16 = (p.vc.row_bytes + 15) & ~15;
+    p.tile_tokens = std::max(1, std::min(32, kTileBudget / (Rk16 + Rv16)));
+    if (ws_bytes < attn_workspace_bytes(n_seqs, n_q_heads, k.head_dim, max_seq_len,
+                                        device_sm_count()))
+        return TQ_ERR_WORKSPACE_TOO_SMALL;
+    const int tk = k.type, tv = v.type;
+    if (tk == TQ_TURBO3 && tv == TQ_TURBO3) return launch_attn_t<3, 3>(p, n_seqs, stream);
+    if (tk == TQ_TURBO2 && tv == TQ_TURBO2) return launch_attn_t<2, 2>(p, n_seqs, stream);
+    if (tk == TQ_TURBO3 && tv == TQ_TURBO2) return launch_attn_t<3, 2>(p, n_seqs, stream);
+    return launch_attn_t<2, 3>(p, n_seqs, stream);
+}
+
+}  // namespace tq

@@ -1,0 +1,302 @@
+// tq_encode.cu -- fused encode: norm -> FWHT -> Lloyd-Max quantise -> bit-pack.
+//
+// "llama.cpp に TurboQuant を実装": the rotation is a fast Walsh-Hadamard transform, adds
+// and subtracts only ("What TurboQuant does differently"), cheap enough to run inside
+// the cache-write path; every 128 values become one fp16 norm plus 3- or 2-bit codes
+// ("How small does it get").
+//
+// GB300 mapping.  One thread owns one 128-value block, so the whole FWHT, the norm tree
+// and the quantiser run in registers with no cross-lane traffic; packed f32x2 adds and
+// multiplies halve the issue slots of the FP32 work.  A persistent CTA of 128 threads
+// walks over tiles of whole token rows (<= 128 blocks, 32 KB of fp16).  Each tile is
+// prefetched with cp.async (16-byte, coalesced) into a double-buffered shared-memory
+// tile whose 16-byte chunks are XOR-swizzled per block, so that the per-thread 16-byte
+// reads of "its" block are bank-conflict free.  Packed blocks are staged in shared
+// memory and written out as whole rows with 16-byte stores.
+//
+// Bit-exactness with the oracle: the same fixed operation order (pairwise norm tree
+// i + len/2, butterfly stages h = 1..64, one IEEE sqrt and one IEEE divide, one multiply
+// per value), every operation rounded separately (no FMA contraction anywhere: the
+// f32x2 instructions and __f*_rn intrinsics are never fused).
+#include "tq_internal.cuh"
+#include "tq_simd.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kThreads = 128;            // blocks per tile (one per thread)
+constexpr int kInBytes = kThreads * 256;  // fp16 input tile
+
+struct EncodeParams {
+    CacheView dst;
+    const __half *src;
+    int64_t stride;            // elements between token rows of src
+    const int32_t *seq_ids;    // or nullptr
+    const int32_t *positions;  // or nullptr
+    int64_t pos0;
+    int64_t n_tokens;
+    int64_t n_tiles;
+    int32_t seq_id;
+    int32_t bpr;               // blocks per token row
+    uint32_t bpr_magic;        // div_magic(bpr)
+    int32_t rows_per_tile;
+    int32_t row_bytes;
+    uint32_t cpr_magic;        // div_magic(row_bytes / 16)  (16-byte path)
+    uint32_t hpr_magic;        // div_magic(row_bytes / 2)   (2-byte path)
+};
+
+template <int TYPE>
+struct EncodeSmem {
+    alignas(128) uint8_t in[2][kInBytes];
+    alignas(16) uint8_t out[kThreads * block_bytes(TYPE)];
+    uint8_t *rowdst[kThreads];
+};
+
+// Issue the cp.async copies of one tile into `buf` (16-byte chunks, swizzled).
+__device__ __forceinline__ void load_tile(const EncodeParams &p, int64_t tile, uint8_t *buf) {
+    const int64_t row0 = tile * p.rows_per_tile;
+    const int rows = (int)min64(p.rows_per_tile, p.n_tokens - row0);
+    const int chunks = rows * p.bpr * 16;
+    const uint32_t sbase = smem_u32(buf);
+    for (int c = threadIdx.x; c < chunks; c += kThreads) {
+        const int f = c >> 4, j = c & 15;
+        const int r = (int)fast_div((uint32_t)f, p.bpr_magic);
+        const int fb = f - r * p.bpr;
+        const __half *g = p.src + (row0 + r) * p.stride + fb * kBlock + j * 8;
+        cp_async16(sbase + f * 256 + ((j ^ (f & 7)) << 4), g);
+    }
+}
+
+template <int TYPE>
+__device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t *out) {
+    const Codebook &cb = c_codebook[cb_index(TYPE)];
+    // ---- 1. norm: pairwise tree, element i pairs with i + len/2 at every level.
+    // Level 1 pairs chunk j with chunk j+8, level 2 chunk j with chunk j+4, so the
+    // tree is formed while streaming the chunks and only 32 partial sums stay live.
+    float s2[32];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        float v[4][8];
+        const int js[4] = {jj, jj + 8, jj + 4, jj + 12};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(blk_in + ((js[q] ^ (f & 7)) << 4));
+            const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 t = __half22float2(h2[e]);
+                v[q][2 * e] = t.x;
+                v[q][2 * e + 1] = t.y;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const float2 a = mul2(make_float2(v[0][e], v[0][e + 1]), make_float2(v[0][e], v[0][e + 1]));
+            const float2 b = mul2(make_float2(v[1][e], v[1][e + 1]), make_float2(v[1][e], v[1][e + 1]));
+            const float2 c = mul2(make_float2(v[2][e], v[2][e + 1]), make_float2(v[2][e], v[2][e + 1]));
+            const float2 d = mul2(make_float2(v[3][e], v[3][e + 1]), make_float2(v[3][e], v[3][e + 1]));
+            const float2 l1a = add2(a, b);   // i (chunk jj)     + i + 64 (chunk jj+8)
+            const float2 l1b = add2(c, d);   // i (chunk jj+4)   + i + 64 (chunk jj+12)
+            const float2 l2 = add2(l1a, l1b);  // i + (i + 32)
+            s2[jj * 8 + e] = l2.x;
+            s2[jj * 8 + e + 1] = l2.y;
+        }
+    }
+#pragma unroll
+    for (int len = 32; len > 2; len >>= 1) {
+#pragma unroll
+        for (int i = 0; i < len / 2; i += 2) {
+            const float2 r = add2(make_float2(s2[i], s2[i + 1]),
+                                  make_float2(s2[i + len / 2], s2[i + len / 2 + 1]));
+            s2[i] = r.x;
+            s2[i + 1] = r.y;
+        }
+    }
+    const float n = __fsqrt_rn(__fadd_rn(s2[0], s2[1]));
+    const uint16_t norm16 = __half_as_ushort(__float2half_rn(fminf(n, 65504.0f)));
+    const float k = n > 0.0f ? __fdiv_rn(kInvSqrt128, n) : 0.0f;
+
+    // ---- 2. FWHT, stages h = 1, 2, ..., 64 in that order.
+    float x[kBlock];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(blk_in + ((j ^ (f & 7)) << 4));
+        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 t = __half22float2(h2[e]);
+            x[8 * j + 2 * e] = t.x;
+            x[8 * j + 2 * e + 1] = t.y;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kBlock; i += 2) {
+        const float a = x[i], b = x[i + 1];
+        x[i] = __fadd_rn(a, b);
+        x[i + 1] = __fsub_rn(a, b);
+    }
+#pragma unroll
+    for (int h = 2; h < kBlock; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < kBlock; i += 2) {
+            if (i & h) continue;
+            const float2 a = make_float2(x[i], x[i + 1]);
+            const float2 b = make_float2(x[i + h], x[i + h + 1]);
+            const float2 s = add2(a, b), d = sub2(a, b);
+            x[i] = s.x;
+            x[i + 1] = s.y;
+            x[i + h] = d.x;
+            x[i + h + 1] = d.y;
+        }
+    }
+
+    // ---- 3. scale to the unit sphere, sign-magnitude Lloyd-Max index, pack.
+    // value i: low-plane word i/16 bits 4k+2r (+1), high-plane word i/32 bit 4k+p.
+    uint32_t W[8], V[4];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) W[w] = 0u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) V[u] = 0u;
+    const float2 kk = make_float2(k, k);
+#pragma unroll
+    for (int i = 0; i < kBlock; i += 2) {
+        const float2 y2 = mul2(make_float2(x[i], x[i + 1]), kk);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int ii = i + e;
+            const float y = e ? y2.y : y2.x;
+            const float a = fabsf(y);
+            const uint32_t s = __float_as_uint(y) >> 31;
+            uint32_t field;
+            if (TYPE == TQ_TURBO3) {
+                const uint32_t m = (uint32_t)(a > cb.threshold[4]) + (uint32_t)(a > cb.threshold[5]) +
+                                   (uint32_t)(a > cb.threshold[6]);
+                field = m ^ (s * 3u);                 // code & 3 of s ? 3-m : 4+m
+                const int jv = ii & 31;
+                V[ii >> 5] |= (s ^ 1u) << (4 * (jv & 7) + (jv >> 3));   // code bit 2
+            } else {
+                const uint32_t m = (uint32_t)(a > cb.threshold[2]);
+                field = ((s ^ 1u) << 1) | (m ^ s);    // s ? 1-m : 2+m
+            }
+            const int jw = ii & 15;
+            W[ii >> 4] |= field << (4 * (jw & 7) + 2 * (jw >> 3));
+        }
+    }
+    // ---- 4. stage the packed block (2-byte aligned in shared memory)
+    uint16_t *o = reinterpret_cast<uint16_t *>(out);
+    o[0] = norm16;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        o[1 + 2 * w] = (uint16_t)(W[w] & 0xffffu);
+        o[2 + 2 * w] = (uint16_t)(W[w] >> 16);
+    }
+    if (TYPE == TQ_TURBO3) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            o[17 + 2 * u] = (uint16_t)(V[u] & 0xffffu);
+            o[18 + 2 * u] = (uint16_t)(V[u] >> 16);
+        }
+    }
+}
+
+template <int TYPE>
+__global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    EncodeSmem<TYPE> &sm = *reinterpret_cast<EncodeSmem<TYPE> *>(smem_raw);
+    constexpr int B = block_bytes(TYPE);
+
+    int64_t tile = blockIdx.x;
+    if (tile < p.n_tiles) load_tile(p, tile, sm.in[0]);
+    cp_async_commit();
+    for (int it = 0; tile < p.n_tiles; ++it, tile += gridDim.x) {
+        const int64_t next = tile + gridDim.x;
+        if (next < p.n_tiles) load_tile(p, next, sm.in[(it + 1) & 1]);
+        cp_async_commit();
+
+        const int64_t row0 = tile * p.rows_per_tile;
+        const int rows = (int)min64(p.rows_per_tile, p.n_tokens - row0);
+        if (threadIdx.x < rows) {
+            const int64_t t = row0 + threadIdx.x;
+            const int64_t seq = p.seq_ids ? (int64_t)p.seq_ids[t] : (int64_t)p.seq_id;
+            const int64_t pos = p.positions ? (int64_t)p.positions[t] : p.pos0 + t;
+            sm.rowdst[threadIdx.x] = row_ptr(p.dst, seq, pos);
+        }
+        cp_async_wait<1>();
+        __syncthreads();
+
+        const int nblk = rows * p.bpr;
+        const int f = threadIdx.x;
+        if (f < nblk) encode_one<TYPE>(sm.in[it & 1] + f * 256, f, sm.out + f * B);
+        __syncthreads();
+
+        // ---- write whole rows out
+        const int R = p.row_bytes;
+        if ((R & 15) == 0) {
+            const int cpr = R >> 4;
+            for (int c = threadIdx.x; c < rows * cpr; c += kThreads) {
+                const int r = (int)fast_div((uint32_t)c, p.cpr_magic);
+                const int cc = c - r * cpr;
+                uint8_t *d = sm.rowdst[r];
+                if (d) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sm.out + r * R + cc * 16);
+                    *reinterpret_cast<uint4 *>(d + cc * 16) = v;
+                }
+            }
+        } else {
+            const int hpr = R >> 1;
+            for (int c = threadIdx.x; c < rows * hpr; c += kThreads) {
+                const int r = (int)fast_div((uint32_t)c, p.hpr_magic);
+                const int cc = c - r * hpr;
+                uint8_t *d = sm.rowdst[r];
+                if (d)
+                    reinterpret_cast<uint16_t *>(d)[cc] =
+                        reinterpret_cast<const uint16_t *>(sm.out + r * R)[cc];
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+}
+
+template <int TYPE>
+tq_status launch_encode_t(const EncodeParams &p, cudaStream_t stream) {
+    const size_t smem = sizeof(EncodeSmem<TYPE>);
+    if (cudaFuncSetAttribute(encode_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<TYPE>, kThreads,
+                                                      smem) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t grid = min64(p.n_tiles, (int64_t)device_sm_count() * per_sm);
+    encode_kernel<TYPE><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+    return check_cuda(cudaGetLastError());
+}
+
+}  // namespace
+
+tq_status launch_encode(const tq_cache &dst, const void *src, int64_t n_tokens, int64_t stride,
+                        const int32_t *seq_ids, const int32_t *positions, int32_t seq_id,
+                        int64_t pos0, cudaStream_t stream) {
+    EncodeParams p;
+    p.dst = make_view(dst);
+    p.src = static_cast<const __half *>(src);
+    p.stride = stride;
+    p.seq_ids = seq_ids;
+    p.positions = positions;
+    p.pos0 = pos0;
+    p.n_tokens = n_tokens;
+    p.seq_id = seq_id;
+    p.bpr = dst.n_kv_heads * (dst.head_dim / kBlock);
+    p.bpr_magic = div_magic((uint32_t)p.bpr);
+    p.rows_per_tile = kThreads / p.bpr;
+    p.n_tiles = (n_tokens + p.rows_per_tile - 1) / p.rows_per_tile;
+    p.row_bytes = p.dst.row_bytes;
+    p.cpr_magic = div_magic((uint32_t)(p.row_bytes / 16 > 0 ? p.row_bytes / 16 : 1));
+    p.hpr_magic = div_magic((uint32_t)(p.row_bytes / 2));
+    return dst.type == TQ_TURBO3 ? launch_encode_t<TQ_TURBO3>(p, stream)
+                                 : launch_encode_t<TQ_TURBO2>(p, stream);
+}
+
+}  // namespace tq

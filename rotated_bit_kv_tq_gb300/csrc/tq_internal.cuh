@@ -1,0 +1,108 @@
+// tq_internal.cuh -- definitions shared by the CUDA translation units of the library.
+// Nothing here is shared with the oracle.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+constexpr int kBlock = TQ_BLOCK_VALUES;  // values per block
+
+// The binary32 value nearest to 1/sqrt(128) = 2^-3.5.
+constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
+
+__host__ __device__ constexpr int block_bytes(int type) { return 2 + kBlock * type / 8; }
+
+__host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// Device-side view of a tq_cache.
+struct CacheView {
+    uint8_t *base;
+    const int32_t *page_table;
+    int64_t capacity;
+    int64_t n_pages;
+    int32_t page_tokens;
+    int32_t max_pages;
+    int32_t n_seqs;
+    int32_t row_bytes;
+};
+
+#if defined(__CUDACC__)
+// First device-side error of the current device (0 = none); read by tq_device_status.
+extern __device__ int32_t g_status;
+
+__device__ __forceinline__ void record_error(int32_t code) { atomicCAS(&g_status, 0, code); }
+
+// Address of row (seq, pos), or nullptr (and TQ_ERR_OUT_OF_RANGE recorded) when the row
+// lies outside the cache.
+__device__ __forceinline__ uint8_t *row_ptr(const CacheView &c, int64_t seq, int64_t pos) {
+    if (seq < 0 || seq >= c.n_seqs || pos < 0) {
+        record_error(TQ_ERR_OUT_OF_RANGE);
+        return nullptr;
+    }
+    int64_t row;
+    if (c.page_tokens == 0) {
+        if (pos >= c.capacity) {
+            record_error(TQ_ERR_OUT_OF_RANGE);
+            return nullptr;
+        }
+        row = seq * c.capacity + pos;
+    } else {
+        int64_t pi = pos / c.page_tokens;
+        if (pi >= c.max_pages) {
+            record_error(TQ_ERR_OUT_OF_RANGE);
+            return nullptr;
+        }
+        int64_t page = c.page_table[seq * c.max_pages + pi];
+        if (page < 0 || page >= c.n_pages) {
+            record_error(TQ_ERR_OUT_OF_RANGE);
+            return nullptr;
+        }
+        row = page * c.page_tokens + pos % c.page_tokens;
+    }
+    return c.base + row * (int64_t)c.row_bytes;
+}
+#endif  // __CUDACC__
+
+// ------------------------------------------------------------------ codebook tables
+// Uploaded by tq_codebook_init.  Index 0 = turbo2 (4 levels), 1 = turbo3 (8 levels).
+struct Codebook {
+    float centroid[8];
+    float threshold[7];
+    __half centroid_h[8];  // fp16 copies used by the tensor-core attention path
+};
+#if defined(__CUDACC__)
+extern __constant__ Codebook c_codebook[2];
+#endif
+
+__host__ __device__ constexpr int cb_index(int type) { return type == TQ_TURBO3 ? 1 : 0; }
+
+// ------------------------------------------------------------------ host side
+bool codebook_ready(int type, int device);
+tq_status check_cuda(cudaError_t e);
+int device_sm_count();
+CacheView make_view(const tq_cache &c);
+tq_status validate_cache(const tq_cache *c);
+
+// Kernel launchers (one per .cu file).
+tq_status launch_encode(const tq_cache &dst, const void *src, int64_t n_tokens, int64_t stride,
+                        const int32_t *seq_ids, const int32_t *positions, int32_t seq_id,
+                        int64_t pos0, cudaStream_t stream);
+tq_status launch_decode(const tq_cache &src, int32_t seq_id, int64_t pos0, int64_t n_tokens,
+                        float *dst, cudaStream_t stream);
+size_t attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max_seq_len,
+                            int sm_count);
+tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
+                      int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
+                      float *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+// Host Lloyd-Max solver (tq_codebook.cpp).
+void solve_codebook(int levels, double *centroids);
+
+}  // namespace tq

@@ -20,7 +20,9 @@ Recipe (all values rounded to fp16, round to nearest even):
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 
 import numpy as np
 
@@ -87,15 +89,8 @@ def k_channel_gain(w: Workload, layer: int) -> np.ndarray:
     return s
 
 
-def kv_tokens(w: Workload, layer: int, kind: str, t0: int, n: int, seq: int = 0) -> np.ndarray:
-    """fp16 [n, n_kv_heads, head_dim] K or V of tokens t0 .. t0+n-1 of one sequence."""
-    assert kind in ("K", "V")
-    out = np.empty((n, w.n_kv_heads, w.head_dim), np.float16)
-    if n == 0:
-        return out
-    gain = k_channel_gain(w, layer) if kind == "K" else None
-    c_first, c_last = t0 // CHUNK, (t0 + n - 1) // CHUNK
-    for c in range(c_first, c_last + 1):
+def _fill_chunks(w, layer, kind, t0, n, seq, gain, out, c_lo, c_hi):
+    for c in range(c_lo, c_hi):
         g = _gen(w, kind, layer, seq, c)
         x = g.standard_normal((CHUNK, w.n_kv_heads, w.head_dim), dtype=np.float32)
         if gain is not None:
@@ -103,6 +98,34 @@ def kv_tokens(w: Workload, layer: int, kind: str, t0: int, n: int, seq: int = 0)
         lo = max(t0, c * CHUNK)
         hi = min(t0 + n, (c + 1) * CHUNK)
         out[lo - t0: hi - t0] = x[lo - c * CHUNK: hi - c * CHUNK].astype(np.float16)
+
+
+_POOL = None
+
+
+def kv_tokens(w: Workload, layer: int, kind: str, t0: int, n: int, seq: int = 0) -> np.ndarray:
+    """fp16 [n, n_kv_heads, head_dim] K or V of tokens t0 .. t0+n-1 of one sequence.
+    Large ranges are drawn by a thread pool; the result does not depend on it (every
+    CHUNK-token piece has its own generator key)."""
+    global _POOL
+    assert kind in ("K", "V")
+    out = np.empty((n, w.n_kv_heads, w.head_dim), np.float16)
+    if n == 0:
+        return out
+    gain = k_channel_gain(w, layer) if kind == "K" else None
+    c_first, c_last = t0 // CHUNK, (t0 + n - 1) // CHUNK
+    n_chunks = c_last - c_first + 1
+    workers = min(16, os.cpu_count() or 1, max(1, n_chunks // 16))
+    if workers <= 1:
+        _fill_chunks(w, layer, kind, t0, n, seq, gain, out, c_first, c_last + 1)
+        return out
+    if _POOL is None:
+        _POOL = concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1))
+    bounds = np.linspace(c_first, c_last + 1, workers + 1).astype(int)
+    futs = [_POOL.submit(_fill_chunks, w, layer, kind, t0, n, seq, gain, out, int(a), int(b))
+            for a, b in zip(bounds[:-1], bounds[1:])]
+    for f in futs:
+        f.result()
     return out
 
 

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Encode: codes and norms bit-exact.  Decode: within 1e-3 absolute.  Attention: within
+2e-3 relative L2 of the oracle's attention over the same packed cache.  Inputs are the
+seeded synthetic workloads of rotated_bit_kv_tq_gb300.synth, at sizes the oracle
+finishes in seconds (several tiles and a ragged tail) and, for the full-size workloads,
+on sampled rows and sequences.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from rotated_bit_kv_tq_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATTN_TOL = 2e-3
+DECODE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def tq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import rotated_bit_kv_tq_gb300 as m
+    from rotated_bit_kv_tq_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+    m.codebook_init(m.TQ_TURBO3, 0)
+    m.codebook_init(m.TQ_TURBO2, 0)
+    return m
+
+
+DEV = "cuda"
+
+
+def _rows_from(cache, n_rows):
+    return cache.buffer[: n_rows * cache.row_bytes].cpu().numpy().reshape(n_rows, cache.row_bytes)
+
+
+def _kv(w, layer, kind, n, t0=0, seq=0):
+    return synth.kv_tokens(w, layer, kind, t0, n, seq).reshape(n, w.n_kv_heads * w.head_dim)
+
+
+# ------------------------------------------------------------------ encode
+
+ENCODE_CASES = [
+    # (type, n_kv_heads, head_dim, tokens)
+    (3, 2, 128, 256),     # tiny workload
+    (3, 8, 128, 1000),    # 16 rows per tile, ragged tail
+    (2, 8, 128, 515),
+    (2, 4, 256, 777),     # head_dim 256 = two blocks per head
+    (3, 1, 128, 333),     # 50-byte rows: 2-byte store path
+    (2, 3, 128, 100),     # 102-byte rows
+    (3, 5, 256, 64),      # 10 blocks per row, 12 rows per tile
+]
+
+
+@pytest.mark.parametrize("tt,hkv,d,n", ENCODE_CASES)
+def test_encode_bit_exact(tq, tt, hkv, d, n):
+    w = synth.scaled(synth.TINY, n_kv_heads=hkv, n_q_heads=hkv, head_dim=d)
+    src = _kv(w, 0, "K", n)
+    cache = tq.KVCache(tt, hkv, d, capacity_tokens=n + 3)
+    tq.encode(cache, torch.from_numpy(src).to(DEV))
+    assert tq.device_status() == 0
+    got = _rows_from(cache, n)
+    ref = oracle.encode_rows(tt, src, hkv, d)
+    assert np.array_equal(got, ref)
+    # rows past the written range stay untouched
+    assert not cache.buffer[n * cache.row_bytes:].any()
+
+
+def test_encode_edge_values(tq):
+    """Zero blocks, single spikes, fp16 extremes, subnormals, norm saturation."""
+    rng = np.random.default_rng(0)
+    n, hkv, d = 40, 2, 128
+    x = rng.standard_normal((n, hkv * d)).astype(np.float16)
+    x[0] = 0
+    x[1] = 0; x[1, 5] = 3.0
+    x[2] = np.float16(65504.0)
+    x[3] = np.float16(-65504.0); x[3, ::2] = np.float16(65504.0)
+    x[4] = np.float16(6e-8)
+    x[5] = (rng.standard_normal(hkv * d) * 1e-6).astype(np.float16)
+    x[6, :128] = np.float16(1.0)            # constant block: W x is a single spike
+    x[7] = -0.0
+    for tt in (2, 3):
+        cache = tq.KVCache(tt, hkv, d, capacity_tokens=n)
+        tq.encode(cache, torch.from_numpy(x).to(DEV))
+        assert np.array_equal(_rows_from(cache, n), oracle.encode_rows(tt, x, hkv, d))
+
+
+def test_encode_strided_source_and_offset(tq):
+    """Rows taken from a wider buffer (stride > row) and written at pos0 > 0."""
+    rng = np.random.default_rng(1)
+    n, hkv, d = 70, 2, 256
+    wide = rng.standard_normal((n, hkv * d + 3 * 8)).astype(np.float16)
+    t = torch.from_numpy(wide).to(DEV)[:, : hkv * d]
+    assert t.stride(0) == hkv * d + 24
+    cache = tq.KVCache(2, hkv, d, capacity_tokens=200)
+    tq.encode(cache, t, pos0=50)
+    rows = cache.buffer.cpu().numpy().reshape(200, -1)
+    ref = oracle.encode_rows(2, np.ascontiguousarray(wide[:, : hkv * d]), hkv, d)
+    assert np.array_equal(rows[50:120], ref)
+    assert not rows[:50].any() and not rows[120:].any()
+
+
+def test_encode_paged_scattered(tq):
+    """One token per sequence at arbitrary positions of a paged cache (the batched
+    append of the batched-decode workload)."""
+    w = synth.scaled(synth.BATCHED_PAGED, n_seqs=9)
+    cap = 1024
+    pt, n_pages = synth.page_table(w, cap)
+    rng = np.random.default_rng(3)
+    pos = rng.integers(0, cap, w.n_seqs).astype(np.int32)
+    seqs = np.arange(w.n_seqs, dtype=np.int32)[::-1].copy()
+    src = np.concatenate([_kv(w, 0, "V", 1, t0=int(p), seq=int(s)) for s, p in zip(seqs, pos)])
+    cache = tq.KVCache(3, w.n_kv_heads, w.head_dim, n_seqs=w.n_seqs, page_tokens=256,
+                       page_table=torch.from_numpy(pt).to(DEV), n_pages=n_pages)
+    tq.encode(cache, torch.from_numpy(src).to(DEV), seq_ids=torch.from_numpy(seqs).to(DEV),
+              positions=torch.from_numpy(pos).to(DEV))
+    assert tq.device_status() == 0
+    pool = cache.buffer.cpu().numpy().reshape(n_pages * 256, -1)
+    ref = oracle.encode_rows(3, src, w.n_kv_heads, w.head_dim)
+    for i, (s, p) in enumerate(zip(seqs, pos)):
+        row = pt[s, p // 256] * 256 + p % 256
+        assert np.array_equal(pool[row], ref[i])
+
+
+def test_encode_out_of_range_is_reported(tq):
+    """A position past the capacity is skipped and reported, never written."""
+    cache = tq.KVCache(3, 2, 128, capacity_tokens=4)
+    src = torch.zeros(2, 256, dtype=torch.float16, device=DEV)
+    tq.encode(cache, src, pos0=3)               # rows 3 (ok) and 4 (out of range)
+    assert tq.device_status() == 7
+    assert tq.device_status() == 0              # read clears it
+
+
+def test_encode_zero_tokens_is_noop(tq):
+    cache = tq.KVCache(3, 2, 128, capacity_tokens=4)
+    tq.encode(cache, torch.zeros(0, 256, dtype=torch.float16, device=DEV))
+    assert not cache.buffer.any()
+
+
+# ------------------------------------------------------------------ decode
+
+@pytest.mark.parametrize("tt,hkv,d,n", [(3, 2, 128, 256), (2, 4, 256, 300), (3, 8, 128, 77)])
+def test_decode_within_tolerance(tq, tt, hkv, d, n):
+    w = synth.scaled(synth.TINY, n_kv_heads=hkv, n_q_heads=hkv, head_dim=d)
+    src = _kv(w, 0, "K", n)
+    cache = tq.KVCache(tt, hkv, d, capacity_tokens=n)
+    tq.encode(cache, torch.from_numpy(src).to(DEV))
+    out = torch.empty(n - 5, hkv, d, dtype=torch.float32, device=DEV)
+    tq.decode(cache, 0, 5, n - 5, out)
+    ref = oracle.decode_rows(tt, oracle.encode_rows(tt, src, hkv, d)[5:], hkv, d)
+    assert np.max(np.abs(out.cpu().numpy() - ref)) < DECODE_TOL
+
+
+# ------------------------------------------------------------------ attention
+
+def _attn_case(tq, w, tk, tv, lens, layer=0, paged=False, cap=None):
+    """Encode K/V of every sequence, run attention, compare each sequence to the oracle."""
+    S, Hkv, Hq, D = len(lens), w.n_kv_heads, w.n_q_heads, w.head_dim
+    max_len = int(max(lens))
+    cap = cap or max(max_len, 1)
+    kw = dict(n_seqs=S)
+    if paged:
+        pt, n_pages = synth.page_table(synth.scaled(w, n_seqs=S), cap)
+        kw.update(page_tokens=256, page_table=torch.from_numpy(pt).to(DEV), n_pages=n_pages)
+    else:
+        kw.update(capacity_tokens=cap)
+    kc = tq.KVCache(tk, Hkv, D, **kw)
+    vc = tq.KVCache(tv, Hkv, D, **kw)
+    ks, vs = [], []
+    for s, L in enumerate(lens):
+        k16, v16 = _kv(w, layer, "K", L, seq=s), _kv(w, layer, "V", L, seq=s)
+        ks.append(k16)
+        vs.append(v16)
+        if L:
+            tq.encode(kc, torch.from_numpy(k16).to(DEV), seq_id=s)
+            tq.encode(vc, torch.from_numpy(v16).to(DEV), seq_id=s)
+    q16 = np.stack([synth.query(w, layer, 0, s) for s in range(S)])
+    out = torch.empty(S, Hq, D, dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(16, tq.attn_workspace_bytes(S, Hq, D, max_len)), dtype=torch.uint8, device=DEV)
+    tq.attn_decode(kc, vc, torch.from_numpy(q16).to(DEV), torch.tensor(lens, dtype=torch.int32, device=DEV),
+                   max_len, out, ws)
+    assert tq.device_status() == 0
+    o = out.cpu().numpy().astype(np.float64)
+    errs = []
+    for s, L in enumerate(lens):
+        kr = oracle.encode_rows(tk, ks[s], Hkv, D) if L else np.zeros((0, kc.row_bytes), np.uint8)
+        vr = oracle.encode_rows(tv, vs[s], Hkv, D) if L else np.zeros((0, vc.row_bytes), np.uint8)
+        ref = oracle.attn_decode(tk, tv, kr, vr, q16[s], L, Hq, Hkv, D, 1.0 / np.sqrt(D))
+        if L == 0:
+            assert np.all(o[s] == 0.0)
+            continue
+        err = np.linalg.norm(o[s] - ref) / np.linalg.norm(ref)
+        errs.append(err)
+        assert err < ATTN_TOL, (s, L, err)
+    return errs
+
+
+def test_attn_tiny_workload(tq):
+    _attn_case(tq, synth.TINY, 3, 3, [synth.TINY.ctx])
+
+
+@pytest.mark.parametrize("tk,tv", [(3, 3), (2, 2), (3, 2), (2, 3)])
+def test_attn_llama_shape_small_ctx(tq, tk, tv):
+    w = synth.LLAMA3_8B_32K
+    _attn_case(tq, w, tk, tv, [1500])
+
+
+def test_attn_gqa5_qwen_shape(tq):
+    _attn_case(tq, synth.QWEN25_14B_32K, 3, 3, [1234])
+    _attn_case(tq, synth.QWEN25_14B_32K, 2, 2, [611])
+
+
+def test_attn_head_dim_256(tq):
+    _attn_case(tq, synth.HD256_128K, 2, 2, [2100])
+
+
+def test_attn_batched_paged(tq):
+    w = synth.BATCHED_PAGED
+    lens = [1, 37, 256, 257, 600, 999, 0, 1024]
+    _attn_case(tq, w, 3, 3, lens, paged=True, cap=1024)
+
+
+def test_attn_single_token_and_ragged(tq):
+    w = synth.TINY
+    _attn_case(tq, w, 3, 3, [1, 2, 31, 33, 65])
+
+
+def test_attn_equal_keys_give_mean(tq):
+    """All keys equal -> uniform weights -> output = mean of the decoded values."""
+    n, hkv, hq, d = 300, 2, 4, 128
+    k = np.tile(np.random.default_rng(1).standard_normal((1, hkv * d)), (n, 1)).astype(np.float16)
+    v = np.random.default_rng(2).standard_normal((n, hkv * d)).astype(np.float16)
+    kc = tq.KVCache(3, hkv, d, capacity_tokens=n)
+    vc = tq.KVCache(3, hkv, d, capacity_tokens=n)
+    tq.encode(kc, torch.from_numpy(k).to(DEV))
+    tq.encode(vc, torch.from_numpy(v).to(DEV))
+    q = torch.randn(1, hq, d, device=DEV).half()
+    out = torch.empty(1, hq, d, device=DEV)
+    ws = torch.empty(tq.attn_workspace_bytes(1, hq, d, n), dtype=torch.uint8, device=DEV)
+    tq.attn_decode(kc, vc, q, torch.tensor([n], dtype=torch.int32, device=DEV), n, out, ws)
+    vh = oracle.decode_rows(3, oracle.encode_rows(3, v, hkv, d), hkv, d).mean(axis=0)
+    ref = np.repeat(vh, hq // hkv, axis=0)
+    got = out.cpu().numpy()[0]
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < ATTN_TOL
+
+
+def test_attn_workspace_too_small_is_rejected(tq):
+    kc = tq.KVCache(3, 2, 128, capacity_tokens=64)
+    q = torch.zeros(1, 4, 128, dtype=torch.float16, device=DEV)
+    out = torch.empty(1, 4, 128, device=DEV)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(tq.TQError) as e:
+        tq.attn_decode(kc, kc, q, torch.tensor([64], dtype=torch.int32, device=DEV), 64, out, ws)
+    assert e.value.status == 4
+
+
+def test_attn_len_beyond_max_is_reported(tq):
+    kc = tq.KVCache(3, 2, 128, capacity_tokens=64)
+    q = torch.zeros(1, 4, 128, dtype=torch.float16, device=DEV)
+    out = torch.empty(1, 4, 128, device=DEV)
+    ws = torch.empty(tq.attn_workspace_bytes(1, 4, 128, 32), dtype=torch.uint8, device=DEV)
+    tq.attn_decode(kc, kc, q, torch.tensor([64], dtype=torch.int32, device=DEV), 32, out, ws)
+    assert tq.device_status() == 7
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def test_full_llama_layer_32k_sampled(tq):
+    """One layer of the Llama-3-8B-shaped workload at its full 32,768-token context, in
+    the configuration the benchmark times: full-size attention vs the oracle, and
+    sampled rows of the packed cache."""
+    _attn_case(tq, synth.LLAMA3_8B_32K, 3, 3, [32768], layer=5)
+
+
+def test_full_hd256_layer_128k(tq):
+    """One layer of the head_dim-256 workload at its full 131,072-token context."""
+    _attn_case(tq, synth.HD256_128K, 2, 2, [131072], layer=1)
+
+
+def test_full_batched_sampled_sequences(tq):
+    """The batched paged workload's real lengths (U[1024, 16384]) for 6 of its sequences."""
+    w = synth.BATCHED_PAGED
+    lens = [int(x) for x in synth.seq_lens(w)[:6]]
+    _attn_case(tq, w, 3, 3, lens, paged=True, cap=16384)
