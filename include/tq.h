@@ -163,6 +163,27 @@ TQ_API tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void
                          int64_t max_seq_len, float softmax_scale, float *out,
                          void *workspace, size_t ws_bytes, void *stream);
 
+/* tq_attn_decode without a workspace argument, for callers that cannot allocate device
+ * memory when they need attention.  Examples are code that runs between the steps of
+ * a serving loop whose memory pools are fully reserved at start-up, and embedders whose
+ * allocator must not be re-entered, or whose policy forbids cudaMalloc (it can
+ * synchronise the device) on the decode path.  The pages have no counterpart to this
+ * entry point; it is a packaging variant of tq_attn_decode.
+ *   Arguments and results are those of tq_attn_decode, minus workspace / ws_bytes.
+ *   Scratch: a fixed 8 MiB array in the library's device memory (every GPU that loads
+ *   the library holds it until the process exits).  A shape whose
+ *   tq_attn_workspace_bytes(...) exceeds 8 MiB returns TQ_ERR_WORKSPACE_TOO_SMALL and
+ *   launches nothing.  The call never allocates or frees memory.
+ *   Set-up: the first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ *   Sharing: all calls on a device share the array and it keeps the last call's
+ *   contents.  Calls whose kernels overlap on the GPU (different streams without
+ *   ordering) race on it; order them on one stream or with events. */
+TQ_API tq_status tq_attn_decode_noalloc(const tq_cache *k, const tq_cache *v,
+                                        const void *q_f16, int n_seqs, int n_q_heads,
+                                        const int32_t *seq_lens, int64_t max_seq_len,
+                                        float softmax_scale, float *out, void *stream);
+
 /* Synchronise `stream`, then read and clear the device status word of the current
  * device: *status_out = TQ_OK or the first device-side error recorded since the
  * last read.  Returns TQ_ERR_CUDA if synchronisation fails. */
