@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTokenAlign = 32;       // split ranges start on multiples of this
+constexpr int kTokenAlign = 16;       // split ranges start on multiples of this
 constexpr int kMaxG = 8;              // query heads per KV head handled in registers
 constexpr int kMaxNb = 2;             // 128-blocks per head handled in registers
 constexpr int kTileBudget = 96 * 1024;  // shared bytes for one K+V tile
@@ -50,7 +50,8 @@ struct SplitPlan {
 
 SplitPlan plan_splits(int n_seqs, int64_t max_len, int sm_count) {
     SplitPlan pl;
-    const int64_t target = max64(1, (2LL * sm_count + n_seqs - 1) / n_seqs);
+    // one wave of one CTA per SM
+    const int64_t target = max64(1, ((int64_t)sm_count + n_seqs - 1) / n_seqs);
     int64_t tps = (max64(max_len, 1) + target - 1) / target;
     tps = (tps + kTokenAlign - 1) / kTokenAlign * kTokenAlign;
     if (tps < kTokenAlign) tps = kTokenAlign;
@@ -359,6 +360,16 @@ size_t partial_smem(const AttnParams &p) {
            16 + (size_t)p.tile_tokens * (Rk16 + Rv16);
 }
 
+tq_status launch_merge(const AttnParams &p, int n_seqs, cudaStream_t stream) {
+    const size_t msmem = sizeof(float) * ((size_t)p.head_dim + (size_t)p.n_splits);
+    if (msmem > 48 * 1024 &&
+        cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)msmem) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    attn_merge_kernel<<<dim3(p.n_q_heads, n_seqs), min(256, p.head_dim), msmem, stream>>>(p);
+    return check_cuda(cudaGetLastError());
+}
+
 template <int TK, int TV>
 tq_status launch_attn_t(const AttnParams &p, int n_seqs, cudaStream_t stream) {
     const size_t smem = partial_smem(p);
@@ -368,13 +379,7 @@ tq_status launch_attn_t(const AttnParams &p, int n_seqs, cudaStream_t stream) {
         return TQ_ERR_CUDA;
     attn_partial_kernel<TK, TV><<<dim3(p.n_splits, n_seqs), kThreads, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
-    const size_t msmem = sizeof(float) * ((size_t)p.head_dim + (size_t)p.n_splits);
-    if (msmem > 48 * 1024 &&
-        cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)msmem) != cudaSuccess)
-        return TQ_ERR_CUDA;
-    attn_merge_kernel<<<dim3(p.n_q_heads, n_seqs), min(256, p.head_dim), msmem, stream>>>(p);
-    return check_cuda(cudaGetLastError());
+    return launch_merge(p, n_seqs, stream);
 }
 
 }  // namespace
@@ -402,7 +407,6 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
     p.group = n_q_heads / k.n_kv_heads;
     p.head_dim = k.head_dim;
     p.nb = k.head_dim / kBlock;
-    if (p.group > kMaxG || p.nb > kMaxNb) return TQ_ERR_UNSUPPORTED;
     if ((size_t)n_q_heads * k.head_dim > 16384) return TQ_ERR_UNSUPPORTED;
     const SplitPlan pl = plan_splits(n_seqs, max_seq_len, device_sm_count());
     p.n_splits = pl.n_splits;
@@ -412,6 +416,13 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
     if (ws_bytes < attn_workspace_bytes(n_seqs, n_q_heads, k.head_dim, max_seq_len,
                                         device_sm_count()))
         return TQ_ERR_WORKSPACE_TOO_SMALL;
+    if (attn_mma_supported(k, v, n_q_heads)) {
+        tq_status st = launch_attn_mma(k, v, q, n_seqs, n_q_heads, seq_lens, max_seq_len, scale,
+                                       p.part, p.n_splits, p.tokens_per_split, stream);
+        if (st != TQ_OK) return st;
+        return launch_merge(p, n_seqs, stream);
+    }
+    if (p.group > kMaxG || p.nb > kMaxNb) return TQ_ERR_UNSUPPORTED;
     const int tk = k.type, tv = v.type;
     if (tk == TQ_TURBO3 && tv == TQ_TURBO3) return launch_attn_t<3, 3>(p, n_seqs, stream);
     if (tk == TQ_TURBO2 && tv == TQ_TURBO2) return launch_attn_t<2, 2>(p, n_seqs, stream);

@@ -102,6 +102,12 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
                       int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
                       float *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+// Tensor-core decode attention (tq_attn_mma.cu): writes split partials like the fp32 kernel.
+bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads);
+tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
+                          int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
+                          float *part, int n_splits, int tokens_per_split, cudaStream_t stream);
+
 // Host Lloyd-Max solver (tq_codebook.cpp).
 void solve_codebook(int levels, double *centroids);
 

@@ -79,16 +79,18 @@ def test_noalloc_matches_workspace_path_twice(tq):
 
 def test_noalloc_rejects_oversized_shape(tq):
     """A shape whose partials exceed the fixed 8 MiB array is refused, not truncated."""
-    kc = tq.KVCache(3, 8, 128, n_seqs=64, capacity_tokens=32)
-    q = torch.zeros(64, 64, 128, dtype=torch.float16, device="cuda")
-    out = torch.zeros(64, 64, 128, device="cuda")
-    lens_t = torch.full((64,), 32, dtype=torch.int32, device="cuda")
-    big = 1 << 22
-    assert tq.attn_workspace_bytes(64, 64, 128, big) > 8 << 20
+    S, Hkv, Hq, D, big = 512, 8, 128, 256, 1 << 20
+    need = tq.attn_workspace_bytes(S, Hq, D, big)
+    assert need > 8 << 20
+    kc = tq.KVCache(3, Hkv, D, n_seqs=S, capacity_tokens=16)
+    q = torch.zeros(S, Hq, D, dtype=torch.float16, device="cuda")
+    out = torch.zeros(S, Hq, D, device="cuda")
+    lens_t = torch.full((S,), 16, dtype=torch.int32, device="cuda")
     lib = tq.load()
     st = lib.tq_attn_decode_noalloc(ctypes.byref(kc.view), ctypes.byref(kc.view),
-                                    ctypes.c_void_p(q.data_ptr()), 64, 64,
+                                    ctypes.c_void_p(q.data_ptr()), S, Hq,
                                     ctypes.c_void_p(lens_t.data_ptr()), big, 0.0,
                                     ctypes.c_void_p(out.data_ptr()), None)
     assert st == 4
+    torch.cuda.synchronize()
     assert not out.any()
