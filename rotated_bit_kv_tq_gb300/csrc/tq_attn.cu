@@ -35,7 +35,7 @@ struct AttnParams {
     CacheView kc, vc;
     const __half *q;
     const int32_t *seq_lens;
-    float *part;   // [n_seqs][n_splits][Hq][D + 2]
+    float *part;   // [n_seqs][n_splits][Hq][part_stride(D)]
     float *out;    // [n_seqs][Hq][D]
     float scale;   // softmax scale (1/sqrt(D) by default)
     int64_t max_len;
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
             for (int hl = 0; hl < kMaxG; ++hl) {
                 if (hl >= G) break;
                 const int h = g * G + hl;
-                float *dst = p.part + (((int64_t)seq * p.n_splits + split) * Hq + h) * (D + 2);
+                float *dst = p.part + (((int64_t)seq * p.n_splits + split) * Hq + h) * part_stride(D);
 #pragma unroll
                 for (int b = 0; b < kMaxNb; ++b) {
                     if (b >= p.nb) break;
@@ -297,60 +297,61 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
     }
 }
 
-// Merge the split partials of one (sequence, head) and undo the rotation.
+// Merge the split partials of one (sequence, head, 128-block) and undo the rotation.
+// Warps take splits round-robin, lanes take four coordinates each (float4 loads of the
+// partial rows), the eight warp sums meet in shared memory, and one warp applies the
+// inverse FWHT with shuffles.
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
-    extern __shared__ __align__(16) float msm[];   // [D] output + [n_splits] weights
-    const int h = blockIdx.x, seq = blockIdx.y, D = p.head_dim, tid = threadIdx.x;
-    float *o = msm;
-    float *wts = msm + D;
-    const float *base = p.part + ((int64_t)seq * p.n_splits * p.n_q_heads + h) * (D + 2);
-    const int64_t sstride = (int64_t)p.n_q_heads * (D + 2);
-    // global max and weights
-    __shared__ float red[32];
+    __shared__ float red_m[8], red_l[8];
+    __shared__ float4 red_o[8][32];
+    const int h = blockIdx.x, seq = blockIdx.y, b = blockIdx.z, D = p.head_dim;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *base = p.part + ((int64_t)seq * p.n_splits * p.n_q_heads + h) * part_stride(D);
+    const int64_t sstride = (int64_t)p.n_q_heads * part_stride(D);
+    // global maximum of the split maxima
     float mx = -INFINITY;
-    for (int s = tid; s < p.n_splits; s += blockDim.x) mx = fmaxf(mx, base[s * sstride + D]);
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if ((tid & 31) == 0) red[tid >> 5] = mx;
+    for (int s = tid; s < p.n_splits; s += 256) mx = fmaxf(mx, base[s * sstride + D]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red_m[warp] = mx;
     __syncthreads();
-    mx = -INFINITY;
-    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) mx = fmaxf(mx, red[w]);
-    __syncthreads();
+    mx = red_m[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red_m[w]);
+    // weighted sums: warp w handles splits w, w+8, ...
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lsum = 0.f;
-    for (int s = tid; s < p.n_splits; s += blockDim.x) {
-        const float m = base[s * sstride + D];
-        const float w = (m == -INFINITY) ? 0.f : __expf(m - mx);
-        wts[s] = w;
-        lsum += w * base[s * sstride + D + 1];
+    for (int s = warp; s < p.n_splits; s += 8) {
+        const float *row = base + s * sstride;
+        const float m = row[D];
+        const float wgt = (m == -INFINITY) ? 0.f : __expf(m - mx);
+        lsum += wgt * row[D + 1];
+        const float4 v = *reinterpret_cast<const float4 *>(row + b * kBlock + 4 * lane);
+        acc.x = fmaf(wgt, v.x, acc.x);
+        acc.y = fmaf(wgt, v.y, acc.y);
+        acc.z = fmaf(wgt, v.z, acc.z);
+        acc.w = fmaf(wgt, v.w, acc.w);
     }
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    if ((tid & 31) == 0) red[tid >> 5] = lsum;
+    red_o[warp][lane] = acc;
+    if (lane == 0) red_l[warp] = lsum;
     __syncthreads();
-    lsum = 0.f;
-    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) lsum += red[w];
-    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-    for (int i = tid; i < D; i += blockDim.x) {
-        float a = 0.f;
-        for (int s = 0; s < p.n_splits; ++s) {
-            const float w = wts[s];
-            if (w != 0.f) a = fmaf(w, base[s * sstride + i], a);
-        }
-        o[i] = a * inv;
+    if (warp != 0) return;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const float4 a = red_o[w][lane];
+        v[0] += a.x;
+        v[1] += a.y;
+        v[2] += a.z;
+        v[3] += a.w;
+        L += red_l[w];
     }
-    __syncthreads();
-    // inverse rotation per 128-block: (1/sqrt(128)) W o_b
-    for (int hlen = 1; hlen < kBlock; hlen <<= 1) {
-        for (int i = tid; i < D; i += blockDim.x) {
-            const int ib = i & (kBlock - 1);
-            if (!(ib & hlen)) {
-                const float a = o[i], b = o[i + hlen];
-                o[i] = a + b;
-                o[i + hlen] = a - b;
-            }
-        }
-        __syncthreads();
-    }
-    float *dst = p.out + ((int64_t)seq * p.n_q_heads + h) * D;
-    for (int i = tid; i < D; i += blockDim.x) dst[i] = o[i] * kInvSqrt128;
+    const float inv = L > 0.f ? kInvSqrt128 / L : 0.f;
+    // inverse rotation (1/sqrt(128)) W o_b, values 4*lane .. 4*lane+3
+    warp_fwht4(v, lane);
+    float4 o4 = make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+    *reinterpret_cast<float4 *>(p.out + ((int64_t)seq * p.n_q_heads + h) * D + b * kBlock + 4 * lane) = o4;
 }
 
 size_t partial_smem(const AttnParams &p) {
@@ -361,12 +362,7 @@ size_t partial_smem(const AttnParams &p) {
 }
 
 tq_status launch_merge(const AttnParams &p, int n_seqs, cudaStream_t stream) {
-    const size_t msmem = sizeof(float) * ((size_t)p.head_dim + (size_t)p.n_splits);
-    if (msmem > 48 * 1024 &&
-        cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)msmem) != cudaSuccess)
-        return TQ_ERR_CUDA;
-    attn_merge_kernel<<<dim3(p.n_q_heads, n_seqs), min(256, p.head_dim), msmem, stream>>>(p);
+    attn_merge_kernel<<<dim3(p.n_q_heads, n_seqs, p.nb), 256, 0, stream>>>(p);
     return check_cuda(cudaGetLastError());
 }
 
@@ -387,7 +383,7 @@ tq_status launch_attn_t(const AttnParams &p, int n_seqs, cudaStream_t stream) {
 size_t attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max_seq_len,
                             int sm_count) {
     const SplitPlan pl = plan_splits(n_seqs, max_seq_len, sm_count);
-    return sizeof(float) * (size_t)n_seqs * pl.n_splits * n_q_heads * (head_dim + 2);
+    return sizeof(float) * (size_t)n_seqs * pl.n_splits * n_q_heads * part_stride(head_dim);
 }
 
 tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,

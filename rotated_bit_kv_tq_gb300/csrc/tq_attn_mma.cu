@@ -31,8 +31,8 @@
 namespace tq {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = 8;
+constexpr int kConsumers = 8;              // compute warps
+constexpr int kThreads = 32 * (kConsumers + 1);   // + one TMA producer warp
 constexpr int kWarpTokens = 64;            // 4 m-tiles of 16 tokens per warp per tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -42,7 +42,7 @@ struct MmaParams {
     CacheView kc, vc;
     const __half *q;
     const int32_t *seq_lens;
-    float *part;        // [n_seqs][n_splits][Hq][D + 2]
+    float *part;        // [n_seqs][n_splits][Hq][part_stride(D)]
     float score_scale;  // softmax scale * log2(e) / sqrt(128)
     int64_t max_len;
     int32_t n_q_heads, n_kv_heads, group, head_dim;
@@ -86,12 +86,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// 32-bit little-endian word at a 2-byte-aligned shared address.
-__device__ __forceinline__ uint32_t ld_u32_2a(const uint8_t *p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t *b = reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3));
-    return __funnelshift_r(b[0], b[1], (uint32_t)(a & 3) * 8u);
-}
 
 __device__ __forceinline__ float ld_norm(const uint8_t *blk) {
     return __half2float(*reinterpret_cast<const __half *>(blk));
@@ -126,13 +120,14 @@ struct HalfTables {
     uint32_t l0, l1, h0, h1;
 };
 
-// Selector of 8 codes: nibble k = code of value (16w + 8r + k) of a block whose low-plane
-// word is W and high-plane word is V (bit 4k+p), per the layout of tq.h.
+// Selector of 8 codes: nibble k = code of value 8r + k (k = 0..7) of a 16-value group whose
+// low-plane word is W, high-plane bit 4k+p of V (layout of tq.h).  Left shifts are
+// integer multiplies so that they issue on the FMA pipe, not the half-rate ALU pipe.
 template <int TYPE>
 __device__ __forceinline__ uint32_t sel8(uint32_t W, uint32_t V, int r, int p) {
     uint32_t x = (r ? (W >> 2) : W) & 0x33333333u;
     if (TYPE == TQ_TURBO3) {
-        const uint32_t hv = (p <= 2) ? (V << (2 - p)) : (V >> (p - 2));
+        const uint32_t hv = p == 0 ? V * 4u : p == 1 ? V * 2u : p == 2 ? V : (V >> 1);
         x |= hv & 0x44444444u;
     }
     return x;
@@ -143,6 +138,49 @@ __device__ __forceinline__ void lookup4(const HalfTables &t, uint32_t sel, uint3
                                         uint32_t &H) {
     L = prmt(t.l0, t.l1, sel);
     H = prmt(t.h0, t.h1, sel);
+}
+
+// The 4 fp16x2 pairs (values 8r+2i, 8r+2i+1 for i = 0..3) of one selector.
+__device__ __forceinline__ void pairs8(const HalfTables &t, uint32_t sel, uint32_t (&o)[4]) {
+    uint32_t L, H, Lh, Hh;
+    lookup4(t, sel, L, H);
+    lookup4(t, __umulhi(sel, 0x10000u), Lh, Hh);   // sel >> 16 on the FMA pipe
+    o[0] = prmt(L, H, 0x5140);
+    o[1] = prmt(L, H, 0x7362);
+    o[2] = prmt(Lh, Hh, 0x5140);
+    o[3] = prmt(Lh, Hh, 0x7362);
+}
+
+// Code words of values 32 q4 .. 32 q4 + 31 of one packed block (2-byte aligned in shared
+// memory; `sh` = 16 when the low-plane words sit at an address = 2 mod 4, else 0; the
+// high-plane words then share that alignment because they start 32 bytes later).
+template <int TYPE>
+struct Quarter {
+    uint32_t W0, W1, V;
+};
+template <int TYPE>
+__device__ __forceinline__ Quarter<TYPE> load_quarter(const uint8_t *blk, int q4, uint32_t sh) {
+    Quarter<TYPE> r;
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(
+        reinterpret_cast<uintptr_t>(blk + 2 + 8 * q4) & ~uintptr_t(3));
+    const uint32_t a = w[0], b = w[1], c = w[2];
+    r.W0 = __funnelshift_r(a, b, sh);
+    r.W1 = __funnelshift_r(b, c, sh);
+    if (TYPE == TQ_TURBO3) {
+        const uint32_t *v = reinterpret_cast<const uint32_t *>(
+            reinterpret_cast<uintptr_t>(blk + 34 + 4 * q4) & ~uintptr_t(3));
+        r.V = __funnelshift_r(v[0], v[1], sh);
+    } else {
+        r.V = 0u;
+    }
+    return r;
+}
+
+// Group (ww, r) of a quarter: the 4 pairs 8ww + 4r + {0..3}.
+template <int TYPE>
+__device__ __forceinline__ void group_pairs(const Quarter<TYPE> &qw, int ww, int r,
+                                            const HalfTables &t, uint32_t (&o)[4]) {
+    pairs8(t, sel8<TYPE>(ww ? qw.W1 : qw.W0, qw.V, r, 2 * ww + r), o);
 }
 
 // Rotate the query of one (head, block) pair held by a warp, four values per lane
@@ -194,6 +232,18 @@ __device__ __forceinline__ void issue_tile(const MmaParams &p, int seq, int64_t 
     asm volatile("mbarrier.arrive.shared.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
 
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Bounded wait on an mbarrier phase; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
 template <int TK, int TV, int NB>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -204,11 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
     const int Rk = p.kc.row_bytes, Rv = p.vc.row_bytes;
     const int TT = p.tile_tokens;
     const int seq = blockIdx.y, split = blockIdx.x;
-    const int g = warp % Hkv, sub = warp / Hkv;
 
     __half *qh = reinterpret_cast<__half *>(smem);                          // [Hq][D]
     const size_t qbytes = ((size_t)Hq * D * 2 + 127) & ~size_t(127);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + qbytes);          // [stages]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + qbytes);          // [stages]
+    uint64_t *empty = full + 4;                                            // [stages]
     uint8_t *stage0 = smem + qbytes + 128;
 
     int64_t len = p.seq_lens[seq];
@@ -221,18 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
     const int n_tiles = t_end > t_begin ? (int)((t_end - t_begin + TT - 1) / TT) : 0;
 
     if (tid == 0) {
-        for (int s = 0; s < p.stages; ++s) mbar_init(smem_u32(&bars[s]), 1);
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-        for (int i = 0; i < n_tiles && i < p.stages; ++i) {
-            const int64_t t0 = t_begin + (int64_t)i * TT;
-            const int nt = (int)min64(TT, t_end - t0);
-            uint8_t *dk = stage0 + (size_t)i * p.stage_bytes;
-            issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&bars[i]));
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), kConsumers);
         }
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-
     // ---- rotate q once per call: qh = fp16(W q_b * scale * log2(e) / sqrt(128))
-    for (int hb = warp; hb < Hq * NB; hb += kWarps) {
+    for (int hb = warp; hb < Hq * NB; hb += kConsumers + 1) {
         const int h = hb / NB, b = hb - h * NB;
         const __half *qp = p.q + ((int64_t)seq * Hq + h) * D + b * kBlock + 4 * lane;
         const uint2 raw = *reinterpret_cast<const uint2 *>(qp);
@@ -247,38 +293,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
     }
     __syncthreads();
 
-    // B fragments of the rotated query: head n = g8 of KV head g, coords 32 q4 + 4 j + e.
-    uint32_t bq[NB][8][2];
-    {
-        const bool hv = g8 < G;
-        const __half *qrow = qh + (g * G + (hv ? g8 : 0)) * D;
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const __half *c = qrow + b * kBlock + 32 * q4 + 4 * j;
-                bq[b][j][0] = hv ? *reinterpret_cast<const uint32_t *>(c) : 0u;
-                bq[b][j][1] = hv ? *reinterpret_cast<const uint32_t *>(c + 2) : 0u;
+    bool timed_out = false;
+    if (warp == kConsumers) {
+        // ================= producer warp: TMA bulk copies of whole row runs
+        if (lane == 0) {
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % p.stages;
+                if (i >= p.stages &&
+                    !mbar_wait(smem_u32(&empty[s]), (uint32_t)(((i / p.stages) - 1) & 1))) {
+                    record_error(TQ_ERR_DEVICE_TIMEOUT);
+                    break;
+                }
+                const int64_t t0 = t_begin + (int64_t)i * TT;
+                const int nt = (int)min64(TT, t_end - t0);
+                uint8_t *dk = stage0 + (size_t)s * p.stage_bytes;
+                issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[s]));
             }
-    }
-    HalfTables tk, tv;
-    {
-        const __half *ck = c_codebook[cb_index(TK)].centroid_h;
-        const __half *cv = c_codebook[cb_index(TV)].centroid_h;
-        uint32_t lk[2] = {0, 0}, hk[2] = {0, 0}, lv[2] = {0, 0}, hv[2] = {0, 0};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint16_t a = e < (1 << TK) ? __half_as_ushort(ck[e]) : 0;
-            const uint16_t c = e < (1 << TV) ? __half_as_ushort(cv[e]) : 0;
-            lk[e >> 2] |= (uint32_t)(a & 0xff) << (8 * (e & 3));
-            hk[e >> 2] |= (uint32_t)(a >> 8) << (8 * (e & 3));
-            lv[e >> 2] |= (uint32_t)(c & 0xff) << (8 * (e & 3));
-            hv[e >> 2] |= (uint32_t)(c >> 8) << (8 * (e & 3));
         }
-        tk = {lk[0], lk[1], hk[0], hk[1]};
-        tv = {lv[0], lv[1], hv[0], hv[1]};
     }
 
+    // ================= consumer warps
+    const int g = warp % Hkv, sub = warp / Hkv;
     float m_run[2] = {-INFINITY, -INFINITY};  // log2 domain, heads 2q4, 2q4+1
     float l_run[2] = {0.f, 0.f};
     float oacc[NB][8][4];
@@ -289,197 +324,149 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
 #pragma unroll
             for (int e = 0; e < 4; ++e) oacc[b][j][e] = 0.f;
 
-    // V-side per-thread constants: low-plane word g8, high-plane word g8/2, bit offset p.
-    const int vp = 2 * (g8 & 1);
-    bool timed_out = false;
-
-    for (int i = 0; i < n_tiles; ++i) {
-        const int s = i % p.stages;
-        const uint32_t bar = smem_u32(&bars[s]);
+    if (warp < kConsumers) {
+        // B fragments of the rotated query: head n = g8 of KV head g, values 32q4 + 4j + e
+        uint32_t bq[NB][8][2];
         {
-            uint32_t it = 0;
-            while (!mbar_try_wait(bar, (uint32_t)((i / p.stages) & 1))) {
-                if (++it > kWaitLimit) {
-                    timed_out = true;
-                    break;
-                }
-            }
-        }
-        // one decision for the whole CTA, so that no thread is left at a barrier
-        timed_out = __syncthreads_or(timed_out) != 0;
-        if (timed_out) {
-            if (tid == 0) record_error(TQ_ERR_DEVICE_TIMEOUT);
-            break;
-        }
-        const int64_t t0 = t_begin + (int64_t)i * TT;
-        const int nt = (int)min64(TT, t_end - t0);
-        const uint8_t *Kt = stage0 + (size_t)s * p.stage_bytes;
-        const uint8_t *Vt = Kt + (size_t)TT * Rk;
-        const int wr0 = sub * kWarpTokens;   // this warp's first row in the tile
-
-        if (wr0 < nt) {
-            // ---------------- scores: S^T[token, head] for 4 m-tiles of 16 tokens
-            float sc[4][4];
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                const int rA = wr0 + 16 * mt + g8, rB = rA + 8;
-                if (wr0 + 16 * mt < nt) {
-                    float acc[NB][4];
-                    float nA[NB], nB[NB];
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[b][e] = 0.f;
-                        const uint8_t *bA = Kt + (size_t)rA * Rk + (g * NB + b) * BK;
-                        const uint8_t *bB = Kt + (size_t)rB * Rk + (g * NB + b) * BK;
-                        nA[b] = ld_norm(bA);
-                        nB[b] = ld_norm(bB);
-                        const uint32_t WA[2] = {ld_u32_2a(bA + 2 + 8 * q4), ld_u32_2a(bA + 6 + 8 * q4)};
-                        const uint32_t WB[2] = {ld_u32_2a(bB + 2 + 8 * q4), ld_u32_2a(bB + 6 + 8 * q4)};
-                        const uint32_t VA = TK == TQ_TURBO3 ? ld_u32_2a(bA + 34 + 4 * q4) : 0u;
-                        const uint32_t VB = TK == TQ_TURBO3 ? ld_u32_2a(bB + 34 + 4 * q4) : 0u;
-#pragma unroll
-                        for (int ww = 0; ww < 2; ++ww)
-#pragma unroll
-                            for (int r = 0; r < 2; ++r) {
-                                const int j0 = 4 * ww + 2 * r;
-                                const uint32_t sA = sel8<TK>(WA[ww], VA, r, 2 * ww + r);
-                                const uint32_t sB = sel8<TK>(WB[ww], VB, r, 2 * ww + r);
-                                uint32_t LA, HA, LB, HB;
-                                lookup4(tk, sA, LA, HA);
-                                lookup4(tk, sB, LB, HB);
-                                mma16816(acc[b], prmt(LA, HA, 0x5140), prmt(LB, HB, 0x5140),
-                                         prmt(LA, HA, 0x7362), prmt(LB, HB, 0x7362), bq[b][j0][0],
-                                         bq[b][j0][1]);
-                                lookup4(tk, sA >> 16, LA, HA);
-                                lookup4(tk, sB >> 16, LB, HB);
-                                mma16816(acc[b], prmt(LA, HA, 0x5140), prmt(LB, HB, 0x5140),
-                                         prmt(LA, HA, 0x7362), prmt(LB, HB, 0x7362),
-                                         bq[b][j0 + 1][0], bq[b][j0 + 1][1]);
-                            }
-                    }
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        s0 = fmaf(nA[b], acc[b][0], s0);
-                        s1 = fmaf(nA[b], acc[b][1], s1);
-                        s2 = fmaf(nB[b], acc[b][2], s2);
-                        s3 = fmaf(nB[b], acc[b][3], s3);
-                    }
-                    const bool okA = t0 + rA < t_end, okB = t0 + rB < t_end;
-                    sc[mt][0] = okA ? s0 : -INFINITY;
-                    sc[mt][1] = okA ? s1 : -INFINITY;
-                    sc[mt][2] = okB ? s2 : -INFINITY;
-                    sc[mt][3] = okB ? s3 : -INFINITY;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[mt][e] = -INFINITY;
-                }
-            }
-            // ---------------- online softmax (log2 domain), heads 2q4 and 2q4+1
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
-                mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
-            }
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-            const float al0 = mn0 == -INFINITY ? 1.f : ex2(m_run[0] - mn0);
-            const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run[1] - mn1);
-            m_run[0] = mn0;
-            m_run[1] = mn1;
-            float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                sc[mt][0] = mn0 == -INFINITY ? 0.f : ex2(sc[mt][0] - mn0);
-                sc[mt][1] = mn1 == -INFINITY ? 0.f : ex2(sc[mt][1] - mn1);
-                sc[mt][2] = mn0 == -INFINITY ? 0.f : ex2(sc[mt][2] - mn0);
-                sc[mt][3] = mn1 == -INFINITY ? 0.f : ex2(sc[mt][3] - mn1);
-                ps0 += sc[mt][0] + sc[mt][2];
-                ps1 += sc[mt][1] + sc[mt][3];
-            }
-            l_run[0] = l_run[0] * al0 + ps0;
-            l_run[1] = l_run[1] * al1 + ps1;
+            const bool hv = g8 < G;
+            const __half *qrow = qh + (g * G + (hv ? g8 : 0)) * D;
 #pragma unroll
             for (int b = 0; b < NB; ++b)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    oacc[b][j][0] *= al0;
-                    oacc[b][j][1] *= al1;
-                    oacc[b][j][2] *= al0;
-                    oacc[b][j][3] *= al1;
+                    const __half *c = qrow + b * kBlock + 32 * q4 + 4 * j;
+                    bq[b][j][0] = hv ? *reinterpret_cast<const uint32_t *>(c) : 0u;
+                    bq[b][j][1] = hv ? *reinterpret_cast<const uint32_t *>(c + 2) : 0u;
                 }
-            // ---------------- values: O^T[coord, head] += C_v^T[coord, token] (p|v|)^T
+        }
+        HalfTables tk, tv;
+        {
+            const __half *ck = c_codebook[cb_index(TK)].centroid_h;
+            const __half *cv = c_codebook[cb_index(TV)].centroid_h;
+            uint32_t lk[2] = {0, 0}, hk[2] = {0, 0}, lv[2] = {0, 0}, hv[2] = {0, 0};
 #pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint16_t a = e < (1 << TK) ? __half_as_ushort(ck[e]) : 0;
+                const uint16_t c = e < (1 << TV) ? __half_as_ushort(cv[e]) : 0;
+                lk[e >> 2] |= (uint32_t)(a & 0xff) << (8 * (e & 3));
+                hk[e >> 2] |= (uint32_t)(a >> 8) << (8 * (e & 3));
+                lv[e >> 2] |= (uint32_t)(c & 0xff) << (8 * (e & 3));
+                hv[e >> 2] |= (uint32_t)(c >> 8) << (8 * (e & 3));
+            }
+            tk = {lk[0], lk[1], hk[0], hk[1]};
+            tv = {lv[0], lv[1], hv[0], hv[1]};
+        }
+        // word alignment of this warp's blocks (same for every row: rows are 16-byte multiples)
+        uint32_t shk[NB], shv[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            shk[b] = (uint32_t)(((g * NB + b) * BK + 2) & 3) * 8u;
+            shv[b] = (uint32_t)(((g * NB + b) * BV + 2) & 3) * 8u;
+        }
+        const int wr0 = sub * kWarpTokens;   // this warp's first row in every tile
+
+        for (int i = 0; i < n_tiles; ++i) {
+            const int s = i % p.stages;
+            if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((i / p.stages) & 1))) {
+                record_error(TQ_ERR_DEVICE_TIMEOUT);
+                timed_out = true;
+                break;
+            }
+            const int64_t t0 = t_begin + (int64_t)i * TT;
+            const int nt = (int)min64(TT, t_end - t0);
+            const uint8_t *Kt = stage0 + (size_t)s * p.stage_bytes;
+            const uint8_t *Vt = Kt + (size_t)TT * Rk;
+#pragma unroll 1
             for (int mt = 0; mt < 4; ++mt) {
-                if (wr0 + 16 * mt >= nt) continue;
-                const int rA = wr0 + 16 * mt + g8, rB = rA + 8;
-                const int rt = wr0 + 16 * mt + 2 * q4;   // first token row of this lane's A pairs
+                const int r16 = wr0 + 16 * mt;
+                if (r16 >= nt) break;
+                const int rA = r16 + g8, rB = rA + 8;
+                const bool okA = t0 + rA < t_end, okB = t0 + rB < t_end;
+                // ---------------- scores S^T[token, head] of this 16-token m-tile
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
-                    const int boff = (g * NB + b) * BV;
-                    const float nvA = ld_norm(Vt + (size_t)rA * Rv + boff);
-                    const float nvB = ld_norm(Vt + (size_t)rB * Rv + boff);
-                    // probabilities of masked tokens are exactly 0; keep stale norms out
-                    const uint32_t x1 = pack_half2(sc[mt][0] == 0.f ? 0.f : sc[mt][0] * nvA,
-                                                   sc[mt][1] == 0.f ? 0.f : sc[mt][1] * nvA);
-                    const uint32_t x2 = pack_half2(sc[mt][2] == 0.f ? 0.f : sc[mt][2] * nvB,
-                                                   sc[mt][3] == 0.f ? 0.f : sc[mt][3] * nvB);
-                    const uint32_t b0 = movtrans(x1), b1 = movtrans(x2);
-                    uint32_t A[2][2][8];   // [token pair][r][m-tile j]
+                    const uint8_t *bA = Kt + (size_t)rA * Rk + (g * NB + b) * BK;
+                    const uint8_t *bB = Kt + (size_t)rB * Rk + (g * NB + b) * BK;
+                    const Quarter<TK> qa = load_quarter<TK>(bA, q4, shk[b]);
+                    const Quarter<TK> qb = load_quarter<TK>(bB, q4, shk[b]);
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int tp = 0; tp < 2; ++tp) {
-                        const uint8_t *v0 = Vt + (size_t)(rt + 8 * tp) * Rv + boff;
-                        const uint8_t *v1 = v0 + Rv;
-                        const uint32_t W0 = ld_u32_2a(v0 + 2 + 4 * g8);
-                        const uint32_t W1 = ld_u32_2a(v1 + 2 + 4 * g8);
-                        uint32_t V0 = 0, V1 = 0;
-                        if (TV == TQ_TURBO3) {
-                            // bit 4k+vp of the high-plane word moved to bit 4k+2
-                            const uint32_t h0 = ld_u32_2a(v0 + 34 + 4 * (g8 >> 1));
-                            const uint32_t h1 = ld_u32_2a(v1 + 34 + 4 * (g8 >> 1));
-                            V0 = __funnelshift_r(h0 << 2, h0 >> 30, vp);
-                            V1 = __funnelshift_r(h1 << 2, h1 >> 30, vp);
-                        }
+                    for (int ww = 0; ww < 2; ++ww)
 #pragma unroll
                         for (int r = 0; r < 2; ++r) {
-                            uint32_t s0 = (r ? (W0 >> 2) : W0) & 0x33333333u;
-                            uint32_t s1 = (r ? (W1 >> 2) : W1) & 0x33333333u;
-                            if (TV == TQ_TURBO3) {
-                                s0 |= (r ? (V0 >> 1) : V0) & 0x44444444u;
-                                s1 |= (r ? (V1 >> 1) : V1) & 0x44444444u;
-                            }
-#pragma unroll
-                            for (int half = 0; half < 2; ++half) {
-                                uint32_t L0, H0, L1, H1;
-                                lookup4(tv, half ? s0 >> 16 : s0, L0, H0);
-                                lookup4(tv, half ? s1 >> 16 : s1, L1, H1);
-                                const uint32_t LL = prmt(L0, L1, 0x5140), HH = prmt(H0, H1, 0x5140);
-                                const uint32_t LL2 = prmt(L0, L1, 0x7362), HH2 = prmt(H0, H1, 0x7362);
-                                A[tp][r][4 * half + 0] = prmt(LL, HH, 0x5140);
-                                A[tp][r][4 * half + 1] = prmt(LL, HH, 0x7362);
-                                A[tp][r][4 * half + 2] = prmt(LL2, HH2, 0x5140);
-                                A[tp][r][4 * half + 3] = prmt(LL2, HH2, 0x7362);
-                            }
+                            uint32_t xa[4], xb[4];
+                            group_pairs<TK>(qa, ww, r, tk, xa);
+                            group_pairs<TK>(qb, ww, r, tk, xb);
+                            const int j = 4 * ww + 2 * r;
+                            mma16816(acc, xa[0], xb[0], xa[1], xb[1], bq[b][j][0], bq[b][j][1]);
+                            mma16816(acc, xa[2], xb[2], xa[3], xb[3], bq[b][j + 1][0], bq[b][j + 1][1]);
                         }
-                    }
+                    const float nA = ld_norm(bA), nB = ld_norm(bB);
+                    s0 = fmaf(nA, acc[0], s0);
+                    s1 = fmaf(nA, acc[1], s1);
+                    s2 = fmaf(nB, acc[2], s2);
+                    s3 = fmaf(nB, acc[3], s3);
+                }
+                s0 = okA ? s0 : -INFINITY;
+                s1 = okA ? s1 : -INFINITY;
+                s2 = okB ? s2 : -INFINITY;
+                s3 = okB ? s3 : -INFINITY;
+                // ---------------- online softmax over these 16 tokens (log2 domain)
+                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        mma16816(oacc[b][j], A[0][0][j], A[0][1][j], A[1][0][j], A[1][1][j], b0, b1);
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+                const float al0 = mn0 == -INFINITY ? 1.f : ex2(m_run[0] - mn0);
+                const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run[1] - mn1);
+                m_run[0] = mn0;
+                m_run[1] = mn1;
+                const float p0 = ex2(s0 - mn0), p1 = ex2(s1 - mn1);   // masked: ex2(-inf) = 0
+                const float p2 = ex2(s2 - mn0), p3 = ex2(s3 - mn1);
+                l_run[0] = l_run[0] * al0 + (p0 + p2);
+                l_run[1] = l_run[1] * al1 + (p1 + p3);
+                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            oacc[b][j][0] *= al0;
+                            oacc[b][j][1] *= al1;
+                            oacc[b][j][2] *= al0;
+                            oacc[b][j][3] *= al1;
+                        }
+                }
+                // ---------------- values O^T[coord, head] += C_v^T[coord, token] (p|v|)^T
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const uint8_t *vA = Vt + (size_t)rA * Rv + (g * NB + b) * BV;
+                    const uint8_t *vB = Vt + (size_t)rB * Rv + (g * NB + b) * BV;
+                    // masked rows may hold stale bytes: their weight is forced to 0
+                    const float nvA = okA ? ld_norm(vA) : 0.f, nvB = okB ? ld_norm(vB) : 0.f;
+                    const uint32_t b0 = movtrans(pack_half2(p0 * nvA, p1 * nvA));
+                    const uint32_t b1 = movtrans(pack_half2(p2 * nvB, p3 * nvB));
+                    const Quarter<TV> qa = load_quarter<TV>(vA, q4, shv[b]);
+                    const Quarter<TV> qb = load_quarter<TV>(vB, q4, shv[b]);
+#pragma unroll
+                    for (int ww = 0; ww < 2; ++ww)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            uint32_t ya[4], yb[4];
+                            group_pairs<TV>(qa, ww, r, tv, ya);
+                            group_pairs<TV>(qb, ww, r, tv, yb);
+                            const int j = 4 * ww + 2 * r;   // m-tiles j, j+1 use pairs 2j..2j+3
+                            mma16816(oacc[b][j], movtrans(ya[0]), movtrans(ya[1]), movtrans(yb[0]),
+                                     movtrans(yb[1]), b0, b1);
+                            mma16816(oacc[b][j + 1], movtrans(ya[2]), movtrans(ya[3]),
+                                     movtrans(yb[2]), movtrans(yb[3]), b0, b1);
+                        }
                 }
             }
-        }
-        __syncthreads();   // every warp is done with stage s
-        if (tid == 0 && i + p.stages < n_tiles) {
-            const int64_t tn = t_begin + (int64_t)(i + p.stages) * TT;
-            const int ntn = (int)min64(TT, t_end - tn);
-            uint8_t *dk = stage0 + (size_t)s * p.stage_bytes;
-            issue_tile(p, seq, tn, ntn, dk, dk + (size_t)TT * Rk, bar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
     }
 
@@ -499,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
         __syncthreads();
         float *xch = reinterpret_cast<float *>(stage0);
         constexpr int kPer = 4 + NB * 32;   // floats per lane
-        if (sub > 0) {
+        if (warp < kConsumers && sub > 0) {
             float *d = xch + ((size_t)warp * 32 + lane) * kPer;
             d[0] = m_run[0];
             d[1] = m_run[1];
@@ -513,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
                     for (int e = 0; e < 4; ++e) d[4 + b * 32 + j * 4 + e] = oacc[b][j][e];
         }
         __syncthreads();
-        if (sub == 0) {
+        if (warp < kConsumers && sub == 0) {
             for (int s2 = 1; s2 < p.wph; ++s2) {
                 const float *d = xch + ((size_t)(s2 * Hkv + g) * 32 + lane) * kPer;
                 float sa[2], sb[2];
@@ -536,18 +523,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
             }
         }
     }
-    if (sub == 0) {
+    if (warp < kConsumers && sub == 0) {
+        // O^T row g8 of m-tile j is value 32(g8/2) + 4j + (g8 & 1) of the block, row g8+8
+        // the value two above it (pairs 2j and 2j+1 after the movmatrix transposes).
+        const int cbase = 32 * (g8 >> 1) + (g8 & 1);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int hl = 2 * q4 + e;
             if (hl >= G) continue;
-            float *dst = p.part + (((int64_t)seq * p.n_splits + split) * Hq + g * G + hl) * (D + 2);
+            float *dst = p.part + (((int64_t)seq * p.n_splits + split) * Hq + g * G + hl) * part_stride(D);
 #pragma unroll
             for (int b = 0; b < NB; ++b)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    dst[b * kBlock + 16 * g8 + j] = oacc[b][j][e];
-                    dst[b * kBlock + 16 * g8 + 8 + j] = oacc[b][j][2 + e];
+                    dst[b * kBlock + cbase + 4 * j] = oacc[b][j][e];
+                    dst[b * kBlock + cbase + 4 * j + 2] = oacc[b][j][2 + e];
                 }
             if (g8 == 0) {
                 dst[D] = m_run[e] == -INFINITY ? -INFINITY : m_run[e] * kLn2;
@@ -576,20 +566,23 @@ tq_status launch_nb(int tk, int tv, const MmaParams &p, int n_seqs, cudaStream_t
     return launch_t<2, 3, NB>(p, n_seqs, stream);
 }
 
+size_t stage_bytes_for(int tile_tokens, size_t rk, size_t rv) {
+    return ((size_t)tile_tokens * (rk + rv) + 16 + 127) & ~size_t(127);
+}
+
 }  // namespace
 
 bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
     const int hkv = k.n_kv_heads, nb = k.head_dim / kBlock, G = n_q_heads / hkv;
-    if (hkv < 1 || hkv > 8 || 8 % hkv) return false;
+    if (hkv < 1 || hkv > kConsumers || kConsumers % hkv) return false;
     if (nb < 1 || nb > 2 || G > 8) return false;
     const size_t rk = tq_row_bytes(k.type, hkv, k.head_dim), rv = tq_row_bytes(v.type, hkv, v.head_dim);
     if (rk % 16 || rv % 16) return false;
-    const int wph = 8 / hkv, TT = kWarpTokens * wph;
+    const int TT = kWarpTokens * (kConsumers / hkv);
     if (k.page_tokens && k.page_tokens % 16) return false;
     if (v.page_tokens && v.page_tokens % 16) return false;
-    const size_t stage = ((size_t)TT * (rk + rv) + 16 + 127) & ~size_t(127);
     const size_t qbytes = ((size_t)n_q_heads * k.head_dim * 2 + 127) & ~size_t(127);
-    return qbytes + 128 + 2 * stage <= 220 * 1024;
+    return qbytes + 128 + 2 * stage_bytes_for(TT, rk, rv) <= 220 * 1024;
 }
 
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
@@ -609,10 +602,9 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     p.head_dim = k.head_dim;
     p.n_splits = n_splits;
     p.tokens_per_split = tokens_per_split;
-    p.wph = 8 / k.n_kv_heads;
+    p.wph = kConsumers / k.n_kv_heads;
     p.tile_tokens = kWarpTokens * p.wph;
-    const size_t stage = ((size_t)p.tile_tokens * (p.kc.row_bytes + p.vc.row_bytes) + 16 + 127) &
-                         ~size_t(127);
+    const size_t stage = stage_bytes_for(p.tile_tokens, p.kc.row_bytes, p.vc.row_bytes);
     p.stage_bytes = (int)stage;
     const size_t qbytes = ((size_t)n_q_heads * k.head_dim * 2 + 127) & ~size_t(127);
     p.stages = (int)std::min<size_t>(4, (220 * 1024 - qbytes - 128) / stage);

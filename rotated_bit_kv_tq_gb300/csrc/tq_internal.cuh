@@ -18,6 +18,10 @@ constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
 
 __host__ __device__ constexpr int block_bytes(int type) { return 2 + kBlock * type / 8; }
 
+// Floats per split-partial row of one (sequence, split, query head): head_dim rotated-domain
+// sums, the running max m, the running sum l, two pad floats (rows stay 16-byte aligned).
+__host__ __device__ constexpr int part_stride(int head_dim) { return head_dim + 4; }
+
 __host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
