@@ -48,15 +48,18 @@ struct SplitPlan {
     int tokens_per_split;
 };
 
-SplitPlan plan_splits(int n_seqs, int64_t max_len, int sm_count) {
+SplitPlan plan_splits(int n_seqs, int head_dim, int64_t max_len, int sm_count) {
     SplitPlan pl;
-    // one wave of one CTA per SM
-    const int64_t target = max64(1, ((int64_t)sm_count + n_seqs - 1) / n_seqs);
+    // one wave: two CTAs per SM with one 128-value block per head, else one
+    const int64_t ctas = (int64_t)sm_count * (head_dim <= kBlock ? 2 : 1);
+    const int64_t target = max64(1, (ctas + n_seqs - 1) / n_seqs);
     int64_t tps = (max64(max_len, 1) + target - 1) / target;
     tps = (tps + kTokenAlign - 1) / kTokenAlign * kTokenAlign;
     if (tps < kTokenAlign) tps = kTokenAlign;
     pl.tokens_per_split = (int)tps;
     pl.n_splits = (int)max64(1, (max_len + tps - 1) / tps);
+    // whole clusters of splits (trailing splits with no tokens write neutral partials)
+    pl.n_splits = (pl.n_splits + kClusterSplits - 1) / kClusterSplits * kClusterSplits;
     return pl;
 }
 
@@ -302,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
 // partial rows), the eight warp sums meet in shared memory, and one warp applies the
 // inverse FWHT with shuffles.
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
+    // launched as a programmatic dependent of the partial kernel: wait for its results
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float red_m[8], red_l[8];
     __shared__ float4 red_o[8][32];
     const int h = blockIdx.x, seq = blockIdx.y, b = blockIdx.z, D = p.head_dim;
@@ -362,8 +367,16 @@ size_t partial_smem(const AttnParams &p) {
 }
 
 tq_status launch_merge(const AttnParams &p, int n_seqs, cudaStream_t stream) {
-    attn_merge_kernel<<<dim3(p.n_q_heads, n_seqs, p.nb), 256, 0, stream>>>(p);
-    return check_cuda(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_q_heads, n_seqs, p.nb);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, attn_merge_kernel, p));
 }
 
 template <int TK, int TV>
@@ -382,7 +395,7 @@ tq_status launch_attn_t(const AttnParams &p, int n_seqs, cudaStream_t stream) {
 
 size_t attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max_seq_len,
                             int sm_count) {
-    const SplitPlan pl = plan_splits(n_seqs, max_seq_len, sm_count);
+    const SplitPlan pl = plan_splits(n_seqs, head_dim, max_seq_len, sm_count);
     return sizeof(float) * (size_t)n_seqs * pl.n_splits * n_q_heads * part_stride(head_dim);
 }
 
@@ -404,7 +417,7 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
     p.head_dim = k.head_dim;
     p.nb = k.head_dim / kBlock;
     if ((size_t)n_q_heads * k.head_dim > 16384) return TQ_ERR_UNSUPPORTED;
-    const SplitPlan pl = plan_splits(n_seqs, max_seq_len, device_sm_count());
+    const SplitPlan pl = plan_splits(n_seqs, k.head_dim, max_seq_len, device_sm_count());
     p.n_splits = pl.n_splits;
     p.tokens_per_split = pl.tokens_per_split;
     const int Rk16 = (p.kc.row_bytes + 15) & ~15, Rv16 = (p.vc.row_bytes + 15) & ~15;
@@ -416,7 +429,9 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
         tq_status st = launch_attn_mma(k, v, q, n_seqs, n_q_heads, seq_lens, max_seq_len, scale,
                                        p.part, p.n_splits, p.tokens_per_split, stream);
         if (st != TQ_OK) return st;
-        return launch_merge(p, n_seqs, stream);
+        AttnParams pm = p;
+        pm.n_splits = p.n_splits / kClusterSplits;   // one partial row per cluster
+        return launch_merge(pm, n_seqs, stream);
     }
     if (p.group > kMaxG || p.nb > kMaxNb) return TQ_ERR_UNSUPPORTED;
     const int tk = k.type, tv = v.type;

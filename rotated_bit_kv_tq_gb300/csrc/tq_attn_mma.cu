@@ -31,12 +31,16 @@
 namespace tq {
 namespace {
 
-constexpr int kConsumers = 8;              // compute warps
-constexpr int kThreads = 32 * (kConsumers + 1);   // + one TMA producer warp
+constexpr int kConsumers = 8;              // compute warps (warp 0 lane 0 also issues TMA)
+constexpr int kThreads = 32 * kConsumers;
 constexpr int kWarpTokens = 64;            // 4 m-tiles of 16 tokens per warp per tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kWaitLimit = 1u << 26;  // bounded mbarrier wait (tens of ms)
+// CTAs per SM aimed for: two (16 warps, 128 registers each, two stages each) with one
+// 128-value block per head; one with two blocks per head.
+__host__ __device__ constexpr int ctas_per_sm(int nb) { return nb == 1 ? 2 : 1; }
+constexpr size_t kSmemBudget = 220 * 1024;   // per SM
 
 struct MmaParams {
     CacheView kc, vc;
@@ -51,6 +55,7 @@ struct MmaParams {
     int32_t tile_tokens;
     int32_t stages;
     int32_t stage_bytes;
+    int32_t cpart_offset;   // bytes from the first stage to this CTA's partial rows
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -245,7 +250,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 
 template <int TK, int TV, int NB>
-__global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p) {
+__global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(const MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int BK = block_bytes(TK), BV = block_bytes(TV);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     // ---- rotate q once per call: qh = fp16(W q_b * scale * log2(e) / sqrt(128))
-    for (int hb = warp; hb < Hq * NB; hb += kConsumers + 1) {
+    for (int hb = warp; hb < Hq * NB; hb += kConsumers) {
         const int h = hb / NB, b = hb - h * NB;
         const __half *qp = p.q + ((int64_t)seq * Hq + h) * D + b * kBlock + 4 * lane;
         const uint2 raw = *reinterpret_cast<const uint2 *>(qp);
@@ -294,23 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
     __syncthreads();
 
     bool timed_out = false;
-    if (warp == kConsumers) {
-        // ================= producer warp: TMA bulk copies of whole row runs
-        if (lane == 0) {
-            for (int i = 0; i < n_tiles; ++i) {
-                const int s = i % p.stages;
-                if (i >= p.stages &&
-                    !mbar_wait(smem_u32(&empty[s]), (uint32_t)(((i / p.stages) - 1) & 1))) {
-                    record_error(TQ_ERR_DEVICE_TIMEOUT);
-                    break;
-                }
-                const int64_t t0 = t_begin + (int64_t)i * TT;
-                const int nt = (int)min64(TT, t_end - t0);
-                uint8_t *dk = stage0 + (size_t)s * p.stage_bytes;
-                issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[s]));
-            }
+    // the first `stages` tiles are in flight before any compute starts
+    if (tid == 0)
+        for (int i = 0; i < n_tiles && i < p.stages; ++i) {
+            const int64_t t0 = t_begin + (int64_t)i * TT;
+            const int nt = (int)min64(TT, t_end - t0);
+            uint8_t *dk = stage0 + (size_t)i * p.stage_bytes;
+            issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i]));
         }
-    }
 
     // ================= consumer warps
     const int g = warp % Hkv, sub = warp / Hkv;
@@ -324,21 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
 #pragma unroll
             for (int e = 0; e < 4; ++e) oacc[b][j][e] = 0.f;
 
-    if (warp < kConsumers) {
-        // B fragments of the rotated query: head n = g8 of KV head g, values 32q4 + 4j + e
-        uint32_t bq[NB][8][2];
-        {
-            const bool hv = g8 < G;
-            const __half *qrow = qh + (g * G + (hv ? g8 : 0)) * D;
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const __half *c = qrow + b * kBlock + 32 * q4 + 4 * j;
-                    bq[b][j][0] = hv ? *reinterpret_cast<const uint32_t *>(c) : 0u;
-                    bq[b][j][1] = hv ? *reinterpret_cast<const uint32_t *>(c + 2) : 0u;
-                }
-        }
+    {
+        // B fragments of the rotated query (head n = g8 of KV head g, values 32q4 + 4j + e)
+        // are read from shared memory at each use: one 8-byte load per k-step.
+        const bool qv = g8 < G;
+        const __half *qrow = qh + (g * G + (qv ? g8 : 0)) * D + 32 * q4;
+        auto bq = [&](int b, int j) -> uint2 {
+            const uint2 v = *reinterpret_cast<const uint2 *>(qrow + b * kBlock + 4 * j);
+            return qv ? v : make_uint2(0u, 0u);
+        };
         HalfTables tk, tv;
         {
             const __half *ck = c_codebook[cb_index(TK)].centroid_h;
@@ -377,43 +367,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
             const uint8_t *Kt = stage0 + (size_t)s * p.stage_bytes;
             const uint8_t *Vt = Kt + (size_t)TT * Rk;
 #pragma unroll 1
-            for (int mt = 0; mt < 4; ++mt) {
-                const int r16 = wr0 + 16 * mt;
-                if (r16 >= nt) break;
-                const int rA = r16 + g8, rB = rA + 8;
-                const bool okA = t0 + rA < t_end, okB = t0 + rB < t_end;
-                // ---------------- scores S^T[token, head] of this 16-token m-tile
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            for (int half = 0; half < 2; ++half) {
+            const int hr0 = wr0 + 32 * half;   // first row of these two m-tiles
+            if (hr0 < nt) {
+                // ---------------- scores S^T[token, head] of two m-tiles (32 tokens)
+                float sc[2][4];
+                // all code words and norms of the phase first, so the loads overlap
+                Quarter<TK> kq[2][NB][2];
+                float kn[2][NB][2];
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const uint8_t *bA = Kt + (size_t)rA * Rk + (g * NB + b) * BK;
-                    const uint8_t *bB = Kt + (size_t)rB * Rk + (g * NB + b) * BK;
-                    const Quarter<TK> qa = load_quarter<TK>(bA, q4, shk[b]);
-                    const Quarter<TK> qb = load_quarter<TK>(bB, q4, shk[b]);
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                    for (int ww = 0; ww < 2; ++ww)
+                    for (int b = 0; b < NB; ++b)
 #pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            uint32_t xa[4], xb[4];
-                            group_pairs<TK>(qa, ww, r, tk, xa);
-                            group_pairs<TK>(qb, ww, r, tk, xb);
-                            const int j = 4 * ww + 2 * r;
-                            mma16816(acc, xa[0], xb[0], xa[1], xb[1], bq[b][j][0], bq[b][j][1]);
-                            mma16816(acc, xa[2], xb[2], xa[3], xb[3], bq[b][j + 1][0], bq[b][j + 1][1]);
+                        for (int t = 0; t < 2; ++t) {
+                            const uint8_t *bk =
+                                Kt + (size_t)(hr0 + 16 * mt + g8 + 8 * t) * Rk + (g * NB + b) * BK;
+                            kq[mt][b][t] = load_quarter<TK>(bk, q4, shk[b]);
+                            kn[mt][b][t] = ld_norm(bk);
                         }
-                    const float nA = ld_norm(bA), nB = ld_norm(bB);
-                    s0 = fmaf(nA, acc[0], s0);
-                    s1 = fmaf(nA, acc[1], s1);
-                    s2 = fmaf(nB, acc[2], s2);
-                    s3 = fmaf(nB, acc[3], s3);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int rA = hr0 + 16 * mt + g8, rB = rA + 8;
+                    float acc[2][4];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const Quarter<TK> &qa = kq[mt][b][0];
+                        const Quarter<TK> &qb = kq[mt][b][1];
+#pragma unroll
+                        for (int ww = 0; ww < 2; ++ww)
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                uint32_t xa[4], xb[4];
+                                group_pairs<TK>(qa, ww, r, tk, xa);
+                                group_pairs<TK>(qb, ww, r, tk, xb);
+                                const int j = 4 * ww + 2 * r;
+                                const uint2 q0 = bq(b, j), q1 = bq(b, j + 1);
+                                mma16816(acc[0], xa[0], xb[0], xa[1], xb[1], q0.x, q0.y);
+                                mma16816(acc[1], xa[2], xb[2], xa[3], xb[3], q1.x, q1.y);
+                            }
+                        const float nA = kn[mt][b][0], nB = kn[mt][b][1];
+                        s0 = fmaf(nA, acc[0][0] + acc[1][0], s0);
+                        s1 = fmaf(nA, acc[0][1] + acc[1][1], s1);
+                        s2 = fmaf(nB, acc[0][2] + acc[1][2], s2);
+                        s3 = fmaf(nB, acc[0][3] + acc[1][3], s3);
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+                    }
+                    // rows past the tile's valid tokens hold stale bytes: masked here
+                    const bool okA = rA < nt, okB = rB < nt;
+                    sc[mt][0] = okA ? s0 : -INFINITY;
+                    sc[mt][1] = okA ? s1 : -INFINITY;
+                    sc[mt][2] = okB ? s2 : -INFINITY;
+                    sc[mt][3] = okB ? s3 : -INFINITY;
                 }
-                s0 = okA ? s0 : -INFINITY;
-                s1 = okA ? s1 : -INFINITY;
-                s2 = okB ? s2 : -INFINITY;
-                s3 = okB ? s3 : -INFINITY;
-                // ---------------- online softmax over these 16 tokens (log2 domain)
-                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                // ---------------- online softmax over the 32 tokens (log2 domain)
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
+                    mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
+                }
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -424,10 +445,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
                 const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run[1] - mn1);
                 m_run[0] = mn0;
                 m_run[1] = mn1;
-                const float p0 = ex2(s0 - mn0), p1 = ex2(s1 - mn1);   // masked: ex2(-inf) = 0
-                const float p2 = ex2(s2 - mn0), p3 = ex2(s3 - mn1);
-                l_run[0] = l_run[0] * al0 + (p0 + p2);
-                l_run[1] = l_run[1] * al1 + (p1 + p3);
+                float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {   // masked: ex2(-inf) = 0
+                    sc[mt][0] = ex2(sc[mt][0] - mn0);
+                    sc[mt][1] = ex2(sc[mt][1] - mn1);
+                    sc[mt][2] = ex2(sc[mt][2] - mn0);
+                    sc[mt][3] = ex2(sc[mt][3] - mn1);
+                    ps0 += sc[mt][0] + sc[mt][2];
+                    ps1 += sc[mt][1] + sc[mt][3];
+                }
+                l_run[0] = l_run[0] * al0 + ps0;
+                l_run[1] = l_run[1] * al1 + ps1;
                 if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
                     for (int b = 0; b < NB; ++b)
@@ -440,33 +469,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
                         }
                 }
                 // ---------------- values O^T[coord, head] += C_v^T[coord, token] (p|v|)^T
+                Quarter<TV> vq[2][NB][2];
+                float vn[2][NB][2];
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const uint8_t *vA = Vt + (size_t)rA * Rv + (g * NB + b) * BV;
-                    const uint8_t *vB = Vt + (size_t)rB * Rv + (g * NB + b) * BV;
-                    // masked rows may hold stale bytes: their weight is forced to 0
-                    const float nvA = okA ? ld_norm(vA) : 0.f, nvB = okB ? ld_norm(vB) : 0.f;
-                    const uint32_t b0 = movtrans(pack_half2(p0 * nvA, p1 * nvA));
-                    const uint32_t b1 = movtrans(pack_half2(p2 * nvB, p3 * nvB));
-                    const Quarter<TV> qa = load_quarter<TV>(vA, q4, shv[b]);
-                    const Quarter<TV> qb = load_quarter<TV>(vB, q4, shv[b]);
+                for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                    for (int ww = 0; ww < 2; ++ww)
+                    for (int b = 0; b < NB; ++b)
 #pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            uint32_t ya[4], yb[4];
-                            group_pairs<TV>(qa, ww, r, tv, ya);
-                            group_pairs<TV>(qb, ww, r, tv, yb);
-                            const int j = 4 * ww + 2 * r;   // m-tiles j, j+1 use pairs 2j..2j+3
-                            mma16816(oacc[b][j], movtrans(ya[0]), movtrans(ya[1]), movtrans(yb[0]),
-                                     movtrans(yb[1]), b0, b1);
-                            mma16816(oacc[b][j + 1], movtrans(ya[2]), movtrans(ya[3]),
-                                     movtrans(yb[2]), movtrans(yb[3]), b0, b1);
+                        for (int t = 0; t < 2; ++t) {
+                            const int row = hr0 + 16 * mt + g8 + 8 * t;
+                            const uint8_t *bv = Vt + (size_t)row * Rv + (g * NB + b) * BV;
+                            vq[mt][b][t] = load_quarter<TV>(bv, q4, shv[b]);
+                            // masked rows may hold stale bytes: their weight is forced to 0
+                            vn[mt][b][t] = row < nt ? ld_norm(bv) : 0.f;
                         }
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const float nvA = vn[mt][b][0], nvB = vn[mt][b][1];
+                        const uint32_t b0 = movtrans(pack_half2(sc[mt][0] * nvA, sc[mt][1] * nvA));
+                        const uint32_t b1 = movtrans(pack_half2(sc[mt][2] * nvB, sc[mt][3] * nvB));
+                        const Quarter<TV> &qa = vq[mt][b][0];
+                        const Quarter<TV> &qb = vq[mt][b][1];
+#pragma unroll
+                        for (int ww = 0; ww < 2; ++ww)
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                uint32_t ya[4], yb[4];
+                                group_pairs<TV>(qa, ww, r, tv, ya);
+                                group_pairs<TV>(qb, ww, r, tv, yb);
+                                const int j = 4 * ww + 2 * r;   // m-tiles j, j+1: pairs 2j..2j+3
+                                mma16816(oacc[b][j], movtrans(ya[0]), movtrans(ya[1]),
+                                         movtrans(yb[0]), movtrans(yb[1]), b0, b1);
+                                mma16816(oacc[b][j + 1], movtrans(ya[2]), movtrans(ya[3]),
+                                         movtrans(yb[2]), movtrans(yb[3]), b0, b1);
+                            }
+                    }
                 }
+            }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            // refill: once every warp has released stage s, bring in tile i + stages
+            if (tid == 0 && i + p.stages < n_tiles) {
+                if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)((i / p.stages) & 1))) {
+                    record_error(TQ_ERR_DEVICE_TIMEOUT);
+                } else {
+                    const int64_t tn = t_begin + (int64_t)(i + p.stages) * TT;
+                    const int ntn = (int)min64(TT, t_end - tn);
+                    uint8_t *dk = stage0 + (size_t)s * p.stage_bytes;
+                    issue_tile(p, seq, tn, ntn, dk, dk + (size_t)TT * Rk, smem_u32(&full[s]));
+                }
+            }
         }
     }
 
@@ -523,7 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
             }
         }
     }
-    if (warp < kConsumers && sub == 0) {
+    // ---------------- this CTA's partial rows [Hq][part_stride(D)] into shared memory
+    // (the end of the stage ring, past the warp exchange area)
+    const int PS = part_stride(D);
+    float *cpart = reinterpret_cast<float *>(stage0 + p.cpart_offset);
+    __syncthreads();
+    if (sub == 0) {
         // O^T row g8 of m-tile j is value 32(g8/2) + 4j + (g8 & 1) of the block, row g8+8
         // the value two above it (pairs 2j and 2j+1 after the movmatrix transposes).
         const int cbase = 32 * (g8 >> 1) + (g8 & 1);
@@ -531,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
         for (int e = 0; e < 2; ++e) {
             const int hl = 2 * q4 + e;
             if (hl >= G) continue;
-            float *dst = p.part + (((int64_t)seq * p.n_splits + split) * Hq + g * G + hl) * part_stride(D);
+            float *dst = cpart + (g * G + hl) * PS;
 #pragma unroll
             for (int b = 0; b < NB; ++b)
 #pragma unroll
@@ -545,6 +605,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(const MmaParams p
             }
         }
     }
+    // ---------------- the CTAs of a cluster (consecutive splits) merge their partials
+    // through distributed shared memory: CTA rank r owns heads r, r + CL, ...
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+    {
+        uint32_t rank;
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+        constexpr int CL = kClusterSplits;
+        const uint32_t local = smem_u32(cpart);
+        const int group = split / CL;
+        const int n_groups = p.n_splits / CL;
+        for (int h = (int)rank + CL * warp; h < Hq; h += CL * kConsumers) {
+            float mc[CL], lc[CL], wgt[CL];
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                uint32_t ra;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                             : "=r"(ra) : "r"(local + (uint32_t)(h * PS + D) * 4u), "r"(c));
+                asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                             : "=f"(mc[c]), "=f"(lc[c]) : "r"(ra) : "memory");
+                M = fmaxf(M, mc[c]);
+            }
+            float L = 0.f;
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                wgt[c] = mc[c] == -INFINITY ? 0.f : __expf(mc[c] - M);
+                L += wgt[c] * lc[c];
+            }
+            float *dst = p.part + (((int64_t)seq * n_groups + group) * Hq + h) * PS;
+            for (int i = 4 * lane; i < D; i += 128) {
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    uint32_t ra;
+                    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                                 : "=r"(ra) : "r"(local + (uint32_t)(h * PS + i) * 4u), "r"(c));
+                    float4 v;
+                    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(ra) : "memory");
+                    a.x = fmaf(wgt[c], v.x, a.x);
+                    a.y = fmaf(wgt[c], v.y, a.y);
+                    a.z = fmaf(wgt[c], v.z, a.z);
+                    a.w = fmaf(wgt[c], v.w, a.w);
+                }
+                *reinterpret_cast<float4 *>(dst + i) = a;
+            }
+            if (lane == 0) {
+                dst[D] = M;
+                dst[D + 1] = L;
+            }
+        }
+    }
+    // let the merge kernel start its launch; it waits for this grid to finish anyway
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // nobody leaves while a peer may still read its shared memory
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
 template <int TK, int TV, int NB>
@@ -554,8 +670,19 @@ tq_status launch_t(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return TQ_ERR_CUDA;
-    attn_mma_kernel<TK, TV, NB><<<dim3(p.n_splits, n_seqs), kThreads, smem, stream>>>(p);
-    return check_cuda(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_splits, n_seqs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterSplits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, attn_mma_kernel<TK, TV, NB>, p));
 }
 
 template <int NB>
@@ -582,7 +709,7 @@ bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
     if (k.page_tokens && k.page_tokens % 16) return false;
     if (v.page_tokens && v.page_tokens % 16) return false;
     const size_t qbytes = ((size_t)n_q_heads * k.head_dim * 2 + 127) & ~size_t(127);
-    return qbytes + 128 + 2 * stage_bytes_for(TT, rk, rv) <= 220 * 1024;
+    return qbytes + 128 + 2 * stage_bytes_for(TT, rk, rv) <= kSmemBudget / ctas_per_sm(nb);
 }
 
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
@@ -607,9 +734,13 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     const size_t stage = stage_bytes_for(p.tile_tokens, p.kc.row_bytes, p.vc.row_bytes);
     p.stage_bytes = (int)stage;
     const size_t qbytes = ((size_t)n_q_heads * k.head_dim * 2 + 127) & ~size_t(127);
-    p.stages = (int)std::min<size_t>(4, (220 * 1024 - qbytes - 128) / stage);
-    if (p.stages < 2) return TQ_ERR_UNSUPPORTED;
     const int nb = k.head_dim / kBlock;
+    p.stages = (int)std::min<size_t>(4, (kSmemBudget / ctas_per_sm(nb) - qbytes - 128) / stage);
+    if (p.stages < 2) return TQ_ERR_UNSUPPORTED;
+    if (n_splits % kClusterSplits) return TQ_ERR_UNSUPPORTED;
+    const size_t cpart = (size_t)n_q_heads * part_stride(k.head_dim) * sizeof(float);
+    if (cpart > (size_t)p.stages * stage) return TQ_ERR_UNSUPPORTED;
+    p.cpart_offset = (int)(((size_t)p.stages * stage - cpart) & ~size_t(15));
     return nb == 1 ? launch_nb<1>(k.type, v.type, p, n_seqs, stream)
                    : launch_nb<2>(k.type, v.type, p, n_seqs, stream);
 }

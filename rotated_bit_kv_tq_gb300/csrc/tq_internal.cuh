@@ -7,7 +7,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/tq.h"
+#include "tq.h"
 
 namespace tq {
 
@@ -17,6 +17,10 @@ constexpr int kBlock = TQ_BLOCK_VALUES;  // values per block
 constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
 
 __host__ __device__ constexpr int block_bytes(int type) { return 2 + kBlock * type / 8; }
+
+// Split-K CTAs of one cluster: the tensor-core attention kernel merges the partials of
+// these consecutive splits in distributed shared memory before writing one row.
+constexpr int kClusterSplits = 2;
 
 // Floats per split-partial row of one (sequence, split, query head): head_dim rotated-domain
 // sums, the running max m, the running sum l, two pad floats (rows stay 16-byte aligned).
