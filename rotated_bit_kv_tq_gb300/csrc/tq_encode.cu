@@ -67,56 +67,17 @@ __device__ __forceinline__ void load_tile(const EncodeParams &p, int64_t tile, u
     }
 }
 
+// Append the sign bit of `v` to a collection word, two positions per value:
+// w = (w << 2) | (bits(v) >> 30).  Every float fed here has |v| < 2, so bit 30 (the top
+// exponent bit) is 0 and each value lands as (sign, 0) at bits (2j+1, 2j).
+__device__ __forceinline__ uint32_t collect2(uint32_t w, float v) {
+    return __funnelshift_l(__float_as_uint(v), w, 2);
+}
+
 template <int TYPE>
 __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t *out) {
     const Codebook &cb = c_codebook[cb_index(TYPE)];
-    // ---- 1. norm: pairwise tree, element i pairs with i + len/2 at every level.
-    // Level 1 pairs chunk j with chunk j+8, level 2 chunk j with chunk j+4, so the
-    // tree is formed while streaming the chunks and only 32 partial sums stay live.
-    float s2[32];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        float v[4][8];
-        const int js[4] = {jj, jj + 8, jj + 4, jj + 12};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 raw = *reinterpret_cast<const uint4 *>(blk_in + ((js[q] ^ (f & 7)) << 4));
-            const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 t = __half22float2(h2[e]);
-                v[q][2 * e] = t.x;
-                v[q][2 * e + 1] = t.y;
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const float2 a = mul2(make_float2(v[0][e], v[0][e + 1]), make_float2(v[0][e], v[0][e + 1]));
-            const float2 b = mul2(make_float2(v[1][e], v[1][e + 1]), make_float2(v[1][e], v[1][e + 1]));
-            const float2 c = mul2(make_float2(v[2][e], v[2][e + 1]), make_float2(v[2][e], v[2][e + 1]));
-            const float2 d = mul2(make_float2(v[3][e], v[3][e + 1]), make_float2(v[3][e], v[3][e + 1]));
-            const float2 l1a = add2(a, b);   // i (chunk jj)     + i + 64 (chunk jj+8)
-            const float2 l1b = add2(c, d);   // i (chunk jj+4)   + i + 64 (chunk jj+12)
-            const float2 l2 = add2(l1a, l1b);  // i + (i + 32)
-            s2[jj * 8 + e] = l2.x;
-            s2[jj * 8 + e + 1] = l2.y;
-        }
-    }
-#pragma unroll
-    for (int len = 32; len > 2; len >>= 1) {
-#pragma unroll
-        for (int i = 0; i < len / 2; i += 2) {
-            const float2 r = add2(make_float2(s2[i], s2[i + 1]),
-                                  make_float2(s2[i + len / 2], s2[i + len / 2 + 1]));
-            s2[i] = r.x;
-            s2[i + 1] = r.y;
-        }
-    }
-    const float n = __fsqrt_rn(__fadd_rn(s2[0], s2[1]));
-    const uint16_t norm16 = __half_as_ushort(__float2half_rn(fminf(n, 65504.0f)));
-    const float k = n > 0.0f ? __fdiv_rn(kInvSqrt128, n) : 0.0f;
-
-    // ---- 2. FWHT, stages h = 1, 2, ..., 64 in that order.
+    // ---- 1. load and convert once
     float x[kBlock];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -129,6 +90,31 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
             x[8 * j + 2 * e + 1] = t.y;
         }
     }
+    // ---- 2. norm: pairwise tree, element i pairs with i + len/2 at every level
+    float s1[64];
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+        const float2 a = mul2(make_float2(x[i], x[i + 1]), make_float2(x[i], x[i + 1]));
+        const float2 b = mul2(make_float2(x[i + 64], x[i + 65]), make_float2(x[i + 64], x[i + 65]));
+        const float2 r = add2(a, b);
+        s1[i] = r.x;
+        s1[i + 1] = r.y;
+    }
+#pragma unroll
+    for (int len = 64; len > 2; len >>= 1) {
+#pragma unroll
+        for (int i = 0; i < len / 2; i += 2) {
+            const float2 r = add2(make_float2(s1[i], s1[i + 1]),
+                                  make_float2(s1[i + len / 2], s1[i + len / 2 + 1]));
+            s1[i] = r.x;
+            s1[i + 1] = r.y;
+        }
+    }
+    const float n = __fsqrt_rn(__fadd_rn(s1[0], s1[1]));
+    const uint16_t norm16 = __half_as_ushort(__float2half_rn(fminf(n, 65504.0f)));
+    const float k = n > 0.0f ? __fdiv_rn(kInvSqrt128, n) : 0.0f;
+
+    // ---- 3. FWHT, stages h = 1, 2, ..., 64 in that order
 #pragma unroll
     for (int i = 0; i < kBlock; i += 2) {
         const float a = x[i], b = x[i + 1];
@@ -149,40 +135,61 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
             x[i + h + 1] = d.y;
         }
     }
-
-    // ---- 3. scale to the unit sphere, sign-magnitude Lloyd-Max index, pack.
-    // value i: low-plane word i/16 bits 4k+2r (+1), high-plane word i/32 bit 4k+p.
-    uint32_t W[8], V[4];
-#pragma unroll
-    for (int w = 0; w < 8; ++w) W[w] = 0u;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) V[u] = 0u;
+    // ---- 4. scale to the unit sphere (|y| <= 1 up to rounding)
     const float2 kk = make_float2(k, k);
 #pragma unroll
     for (int i = 0; i < kBlock; i += 2) {
         const float2 y2 = mul2(make_float2(x[i], x[i + 1]), kk);
+        x[i] = y2.x;
+        x[i + 1] = y2.y;
+    }
+    // ---- 5. sign-magnitude Lloyd-Max index, bit-parallel.
+    // "|y| > t" is the sign bit of fl(t - |y|) (exact zero only when |y| == t, which is
+    // not "greater"); sign(y) is the sign bit of y.  Low-plane word w holds value
+    // i = 16w + 8r + k at bits 4k+2r (code bit 0) and 4k+2r+1 (code bit 1): collecting
+    // values in the order j = 2k + r, last first, puts value j's predicate at bit 2j+1.
+    uint32_t W[8], SP[8];
+    const float t_lo = TYPE == TQ_TURBO3 ? cb.threshold[4] : cb.threshold[2];
+    const float t_mid = TYPE == TQ_TURBO3 ? cb.threshold[5] : 0.0f;
+    const float t_hi = TYPE == TQ_TURBO3 ? cb.threshold[6] : 0.0f;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int ii = i + e;
-            const float y = e ? y2.y : y2.x;
+    for (int w = 0; w < 8; ++w) {
+        uint32_t ps = 0, p4 = 0, p5 = 0, p6 = 0;
+#pragma unroll
+        for (int j = 15; j >= 0; --j) {
+            const float y = x[16 * w + 8 * (j & 1) + (j >> 1)];
             const float a = fabsf(y);
-            const uint32_t s = __float_as_uint(y) >> 31;
-            uint32_t field;
+            ps = collect2(ps, y);
+            p4 = collect2(p4, __fsub_rn(t_lo, a));
             if (TYPE == TQ_TURBO3) {
-                const uint32_t m = (uint32_t)(a > cb.threshold[4]) + (uint32_t)(a > cb.threshold[5]) +
-                                   (uint32_t)(a > cb.threshold[6]);
-                field = m ^ (s * 3u);                 // code & 3 of s ? 3-m : 4+m
-                const int jv = ii & 31;
-                V[ii >> 5] |= (s ^ 1u) << (4 * (jv & 7) + (jv >> 3));   // code bit 2
-            } else {
-                const uint32_t m = (uint32_t)(a > cb.threshold[2]);
-                field = ((s ^ 1u) << 1) | (m ^ s);    // s ? 1-m : 2+m
+                p5 = collect2(p5, __fsub_rn(t_mid, a));
+                p6 = collect2(p6, __fsub_rn(t_hi, a));
             }
-            const int jw = ii & 15;
-            W[ii >> 4] |= field << (4 * (jw & 7) + 2 * (jw >> 3));
+        }
+        if (TYPE == TQ_TURBO3) {
+            // m = (|y|>t4) + (|y|>t5) + (|y|>t6): bit1 = |y|>t5, bit0 = |y|>(bit1 ? t6 : t4);
+            // code & 3 = m ^ 3s  -> fields (bit1 ^ s, bit0 ^ s)
+            const uint32_t b0 = (p5 & p6) | (~p5 & p4);
+            W[w] = (p5 ^ ps) | ((b0 ^ ps) >> 1);
+        } else {
+            // code = s ? 1 - m : 2 + m  -> fields (!s, m ^ s)
+            W[w] = (~ps & 0xAAAAAAAAu) | ((p4 ^ ps) >> 1);
+        }
+        SP[w] = ps;
+    }
+    // high plane (turbo3): code bit 2 = !s.  Word u gathers values 32u + 16w' + 8r + k at
+    // bit 4k + 2w' + r; the sign of value (w = 2u + w', r, k) sits at bit 4k + 2r + 1.
+    uint32_t V[4];
+    if (TYPE == TQ_TURBO3) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t a = SP[2 * u], b = SP[2 * u + 1];
+            const uint32_t sv = ((a & 0x22222222u) >> 1) | ((a & 0x88888888u) >> 2) |
+                                ((b & 0x22222222u) << 1) | (b & 0x88888888u);
+            V[u] = ~sv;
         }
     }
-    // ---- 4. stage the packed block (2-byte aligned in shared memory)
+    // ---- 6. stage the packed block (2-byte aligned in shared memory)
     uint16_t *o = reinterpret_cast<uint16_t *>(out);
     o[0] = norm16;
 #pragma unroll
