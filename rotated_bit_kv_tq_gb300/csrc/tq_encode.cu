@@ -207,7 +207,7 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
 }
 
 template <int TYPE>
-__global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3) encode_kernel(const EncodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem<TYPE> &sm = *reinterpret_cast<EncodeSmem<TYPE> *>(smem_raw);
     constexpr int B = block_bytes(TYPE);
