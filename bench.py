@@ -36,6 +36,12 @@ from rotated_bit_kv_tq_gb300 import synth  # noqa: E402
 
 DECODE_STEPS = 128
 
+# DRAM bytes per token measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
+# 262,144-token probe of the same kernels (profiles/*_262k.md), scaled to a launch by its
+# token count: attention reads every packed row once, encode reads fp16 and writes packed rows,
+# so traffic grows in proportion to tokens.  None once a kernel changes after its capture.
+TRAFFIC_PER_TOKEN = {"attn": 212.84e6 / 262144, "encode": 628.07e6 / 262144}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -45,6 +51,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=synth.LLAMA3_8B_32K.name,
                     choices=[w.name for w in synth.WORKLOADS])
+    ap.add_argument("--kernel-probe", type=int, default=0, metavar="CTX",
+                    help="time one layer's encode and attention at context CTX (the small "
+                         "case the ncu captures use) instead of the full benchmark")
     return ap.parse_args()
 
 
@@ -128,6 +137,21 @@ def measured_peak_hbm():
         with open(p) as f:
             return float(json.load(f)["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ multi-rank timing
+
+def reduce_max(values, dist, device):
+    """Max over ranks of per-rank timings (the slowest replica sets the job's time)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world, units_per_rank, max_ms):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / (max_ms / 1e3)
 
 
 # ------------------------------------------------------------------ inputs
@@ -289,17 +313,14 @@ def run_ours(args, rank, world, local_rank, dist):
     assert np.isfinite(out_host.numpy()).all()
 
     if dist:
-        import torch.distributed as tdist
-        t = torch.tensor([pre_ms, dec_ms, e2e_pre_ms, e2e_dec_ms], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        pre_ms, dec_ms, e2e_pre_ms, e2e_dec_ms = t.tolist()
+        pre_ms, dec_ms, e2e_pre_ms, e2e_dec_ms = reduce_max(
+            [pre_ms, dec_ms, e2e_pre_ms, e2e_dec_ms], dist, dev)
     if rank != 0:
         return
 
     K = args.steps
     enc_bytes = encode_bytes_per_token(w, tt) * T * L
-    tokens = world * K * S
-    value = tokens / (dec_ms / 1e3)
+    value = job_throughput(world, K * S, dec_ms)
     enc_gbs = world * K * enc_bytes / (pre_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak_hbm()
     a_bytes = attn_bytes(w, max_len, tt)
@@ -331,11 +352,13 @@ def run_ours(args, rank, world, local_rank, dist):
         "decode_ms_per_step": dec_ms / K,
         "roofline": {"kernel": "tq_attn_decode (split-K partial + merge)", "bound": "hbm",
                      "achieved": a_gbs, "peak": peak, "unit": "GB/s", "frac": a_gbs / peak,
-                     "peak_source": peak_kind, "traffic": None,
+                     "peak_source": peak_kind,
+                     "traffic": TRAFFIC_PER_TOKEN["attn"] * max_len if TRAFFIC_PER_TOKEN["attn"] else None,
                      "bytes_per_launch": a_bytes, "launch_ms": attn_launch_ms},
         "encode_roofline": {"kernel": "tq_encode (prefill, one layer, K)", "bound": "hbm",
                             "achieved": e_gbs, "peak": peak, "unit": "GB/s", "frac": e_gbs / peak,
                             "peak_source": peak_kind, "bytes_per_launch": e_bytes,
+                            "traffic": TRAFFIC_PER_TOKEN["encode"] * T if TRAFFIC_PER_TOKEN["encode"] else None,
                             "launch_ms": enc_launch_ms},
         "e2e": {"value": world * n_e2e * S / (e2e_dec_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -412,8 +435,54 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def kernel_probe(args):
+    """One layer of the workload's shape at context args.kernel_probe: encode of K and V,
+    then repeated decode attention; per-call times from CUDA events (not a bench line)."""
+    import torch
+    import rotated_bit_kv_tq_gb300 as tq
+    from rotated_bit_kv_tq_gb300 import build
+    build.build()
+    w = workload(args.workload)
+    tt = w.types[0]
+    tq.codebook_init(tt, 0)
+    ctx, Hkv, Hq, D = args.kernel_probe, w.n_kv_heads, w.n_q_heads, w.head_dim
+    k16 = torch.from_numpy(synth.kv_tokens(w, 0, "K", 0, ctx).reshape(ctx, -1)).cuda()
+    v16 = torch.from_numpy(synth.kv_tokens(w, 0, "V", 0, ctx).reshape(ctx, -1)).cuda()
+    kc = tq.KVCache(tt, Hkv, D, capacity_tokens=ctx)
+    vc = tq.KVCache(tt, Hkv, D, capacity_tokens=ctx)
+    q = torch.from_numpy(synth.query(w, 0, 0)).cuda().reshape(1, Hq, D)
+    out = torch.empty(1, Hq, D, device="cuda")
+    lens = torch.tensor([ctx], dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(16, tq.attn_workspace_bytes(1, Hq, D, ctx)), dtype=torch.uint8, device="cuda")
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    for _ in range(3):
+        tq.encode(kc, k16)
+        tq.encode(vc, v16)
+        tq.attn_decode(kc, vc, q, lens, ctx, out, ws)
+    torch.cuda.synchronize()
+    enc_ms = timed(lambda: tq.encode(kc, k16), 10)
+    att_ms = timed(lambda: tq.attn_decode(kc, vc, q, lens, ctx, out, ws), 20)
+    enc_b = ctx * (Hkv * D * 2 + kc.row_bytes)
+    att_b = attn_bytes(w, ctx, tt)
+    print(json.dumps({"probe": w.name, "ctx": ctx, "encode_us": enc_ms * 1e3,
+                      "encode_gbs": enc_b / enc_ms / 1e6, "attn_us": att_ms * 1e3,
+                      "attn_gbs": att_b / att_ms / 1e6, "status": tq.device_status()}))
+
+
 def main():
     args = parse()
+    if args.kernel_probe:
+        kernel_probe(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

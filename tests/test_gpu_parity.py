@@ -287,3 +287,34 @@ def test_full_batched_sampled_sequences(tq):
     w = synth.BATCHED_PAGED
     lens = [int(x) for x in synth.seq_lens(w)[:6]]
     _attn_case(tq, w, 3, 3, lens, paged=True, cap=16384)
+
+
+def test_full_qwen14b_layer_32k_both_types(tq):
+    """The Qwen2.5-14B-shaped workload (8 KV heads, 40 query heads: G = 5) at its full
+    32,768-token context, run once with turbo3 and once with turbo2 on identical data."""
+    w = synth.QWEN25_14B_32K
+    _attn_case(tq, w, 3, 3, [32768], layer=7)
+    _attn_case(tq, w, 2, 2, [32768], layer=7)
+
+
+def test_qwen14b_bytes_freed_and_mse(tq):
+    """Bytes freed against FP16 ('Why the KV cache is so heavy' size formula) and the
+    quantisation error per type, K and V separately, on one full-context layer."""
+    w = synth.QWEN25_14B_32K
+    T = w.ctx
+    fp16 = oracle.kv_bytes(w.layers, w.n_kv_heads, w.head_dim, T, 2, 1)
+    for tt, mse_lo, mse_hi in ((3, 0.025, 0.045), (2, 0.09, 0.14)):
+        cache = tq.KVCache(tt, w.n_kv_heads, w.head_dim, capacity_tokens=T)
+        # allocated bytes of all layers' K and V equal the formula at 50/128 or 34/128 B/value
+        allocated = 2 * w.layers * cache.nbytes
+        assert allocated == oracle.kv_bytes(w.layers, w.n_kv_heads, w.head_dim, T,
+                                            oracle.block_bytes(tt), 128)
+        assert fp16 - allocated == {3: 4944, 2: 5328}[tt] * 2 ** 20
+        for kind in ("K", "V"):
+            x = torch.from_numpy(_kv(w, 3, kind, T)).to(DEV)
+            tq.encode(cache, x)
+            xh = torch.empty(T, w.n_kv_heads, w.head_dim, device=DEV)
+            tq.decode(cache, 0, 0, T, xh)
+            xf = x.float().reshape(T, w.n_kv_heads, w.head_dim)
+            nmse = float(((xf - xh) ** 2).sum() / (xf ** 2).sum())
+            assert mse_lo < nmse < mse_hi, (tt, kind, nmse)
