@@ -130,6 +130,17 @@ TQ_API tq_status tq_encode(const tq_cache *dst, const void *src_f16, int64_t n_t
                     const int32_t *positions, int32_t seq_id, int64_t pos0,
                     void *stream);
 
+/* tq_encode of the K rows into `k` and of the V rows into `v` in one launch (K and V
+ * are quantised independently, "How to use": -ctk / -ctv; the decode step appends both
+ * before attending, kenji.blog article section 8).  Arguments as for tq_encode, per
+ * cache; seq_ids / positions / seq_id / pos0 apply to both.  Caches of different types
+ * are encoded by two launches. */
+TQ_API tq_status tq_encode_kv(const tq_cache *k, const tq_cache *v, const void *k_src_f16,
+                              const void *v_src_f16, int64_t n_tokens, int64_t k_token_stride,
+                              int64_t v_token_stride, const int32_t *seq_ids,
+                              const int32_t *positions, int32_t seq_id, int64_t pos0,
+                              void *stream);
+
 /* Dequantise rows pos0 .. pos0+n_tokens-1 of sequence seq_id to fp32
  * dst [n_tokens][n_kv_heads][head_dim] (device): x_hat = norm * W c / sqrt(128)
  * ("What TurboQuant does differently": the rotation is undone at read time). */

@@ -12,7 +12,7 @@ import ctypes
 from ._lib import (TQ_BLOCK_VALUES, TQ_TURBO2, TQ_TURBO3, TQError, TqCache, check, load)
 
 __all__ = ["TQ_TURBO2", "TQ_TURBO3", "TQ_BLOCK_VALUES", "TQError", "TqCache", "KVCache",
-           "block_bytes", "row_bytes", "codebook_init", "codebook_get", "encode", "decode",
+           "block_bytes", "row_bytes", "codebook_init", "codebook_get", "encode", "encode_kv", "decode",
            "attn_workspace_bytes", "attn_decode", "device_status", "load"]
 
 
@@ -85,6 +85,19 @@ def encode(cache: KVCache, src, *, seq_ids=None, positions=None, seq_id: int = 0
     stride = src.stride(0) if src.dim() > 1 else cache.n_kv_heads * cache.head_dim
     check(load().tq_encode(ctypes.byref(cache.view), _ptr(src), n, stride, _ptr(seq_ids),
                            _ptr(positions), seq_id, pos0, _stream_ptr(stream)), "tq_encode")
+
+
+def encode_kv(kc: KVCache, vc: KVCache, k_src, v_src, *, seq_ids=None, positions=None,
+              seq_id: int = 0, pos0: int = 0, stream=None):
+    """K rows into kc and V rows into vc in one launch (same arguments as encode)."""
+    n = k_src.shape[0]
+    if v_src.shape[0] != n:
+        raise TQError(1, "encode_kv: K and V token counts differ")
+    ks = k_src.stride(0) if k_src.dim() > 1 else kc.n_kv_heads * kc.head_dim
+    vs = v_src.stride(0) if v_src.dim() > 1 else vc.n_kv_heads * vc.head_dim
+    check(load().tq_encode_kv(ctypes.byref(kc.view), ctypes.byref(vc.view), _ptr(k_src),
+                              _ptr(v_src), n, ks, vs, _ptr(seq_ids), _ptr(positions), seq_id,
+                              pos0, _stream_ptr(stream)), "tq_encode_kv")
 
 
 def decode(cache: KVCache, seq_id: int, pos0: int, n_tokens: int, out, stream=None):

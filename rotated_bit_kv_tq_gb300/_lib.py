@@ -55,6 +55,11 @@ SIGNATURES = {
     "tq_encode": (ctypes.c_int, [ctypes.POINTER(TqCache), ctypes.c_void_p, ctypes.c_int64,
                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                  ctypes.c_int64, ctypes.c_void_p]),
+    "tq_encode_kv": (ctypes.c_int, [ctypes.POINTER(TqCache), ctypes.POINTER(TqCache),
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                    ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                    ctypes.c_void_p]),
     "tq_decode": (ctypes.c_int, [ctypes.POINTER(TqCache), ctypes.c_int32, ctypes.c_int64,
                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
     "tq_attn_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,

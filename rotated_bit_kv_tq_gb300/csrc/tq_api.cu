@@ -149,6 +149,31 @@ tq_status tq_encode(const tq_cache *dst, const void *src_f16, int64_t n_tokens,
                          pos0, static_cast<cudaStream_t>(stream));
 }
 
+tq_status tq_encode_kv(const tq_cache *k, const tq_cache *v, const void *k_src_f16,
+                       const void *v_src_f16, int64_t n_tokens, int64_t k_token_stride,
+                       int64_t v_token_stride, const int32_t *seq_ids, const int32_t *positions,
+                       int32_t seq_id, int64_t pos0, void *stream) {
+    tq_status st = validate_cache(k);
+    if (st != TQ_OK) return st;
+    st = validate_cache(v);
+    if (st != TQ_OK) return st;
+    if (n_tokens < 0) return TQ_ERR_INVALID_ARGUMENT;
+    if (n_tokens == 0) return TQ_OK;
+    if (!k_src_f16 || reinterpret_cast<uintptr_t>(k_src_f16) % 16 || !v_src_f16 ||
+        reinterpret_cast<uintptr_t>(v_src_f16) % 16)
+        return TQ_ERR_INVALID_ARGUMENT;
+    if (k_token_stride < (int64_t)k->n_kv_heads * k->head_dim || k_token_stride % 8 ||
+        v_token_stride < (int64_t)v->n_kv_heads * v->head_dim || v_token_stride % 8)
+        return TQ_ERR_INVALID_ARGUMENT;
+    if (!positions && pos0 < 0) return TQ_ERR_INVALID_ARGUMENT;
+    if (!seq_ids && (seq_id < 0 || seq_id >= k->n_seqs || seq_id >= v->n_seqs))
+        return TQ_ERR_INVALID_ARGUMENT;
+    if (n_tokens > (int64_t)1 << 40) return TQ_ERR_UNSUPPORTED;
+    return launch_encode_kv(*k, *v, k_src_f16, v_src_f16, n_tokens, k_token_stride,
+                            v_token_stride, seq_ids, positions, seq_id, pos0,
+                            static_cast<cudaStream_t>(stream));
+}
+
 tq_status tq_decode(const tq_cache *src, int32_t seq_id, int64_t pos0, int64_t n_tokens,
                     float *dst, void *stream) {
     tq_status st = validate_cache(src);

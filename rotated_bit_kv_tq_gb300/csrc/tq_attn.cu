@@ -323,19 +323,33 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     mx = red_m[0];
 #pragma unroll
     for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red_m[w]);
-    // weighted sums: warp w handles splits w, w+8, ...
+    // weighted sums: warp w handles splits w, w+8, ...; four rows in flight at a time
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lsum = 0.f;
-    for (int s = warp; s < p.n_splits; s += 8) {
-        const float *row = base + s * sstride;
-        const float m = row[D];
-        const float wgt = (m == -INFINITY) ? 0.f : __expf(m - mx);
-        lsum += wgt * row[D + 1];
-        const float4 v = *reinterpret_cast<const float4 *>(row + b * kBlock + 4 * lane);
-        acc.x = fmaf(wgt, v.x, acc.x);
-        acc.y = fmaf(wgt, v.y, acc.y);
-        acc.z = fmaf(wgt, v.z, acc.z);
-        acc.w = fmaf(wgt, v.w, acc.w);
+    for (int s0 = warp; s0 < p.n_splits; s0 += 32) {
+        float2 ml[4];
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int s = s0 + 8 * u;
+            if (s < p.n_splits) {
+                const float *row = base + s * sstride;
+                ml[u] = *reinterpret_cast<const float2 *>(row + D);
+                v[u] = *reinterpret_cast<const float4 *>(row + b * kBlock + 4 * lane);
+            } else {
+                ml[u] = make_float2(-INFINITY, 0.f);
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float wgt = (ml[u].x == -INFINITY) ? 0.f : __expf(ml[u].x - mx);
+            lsum += wgt * ml[u].y;
+            acc.x = fmaf(wgt, v[u].x, acc.x);
+            acc.y = fmaf(wgt, v[u].y, acc.y);
+            acc.z = fmaf(wgt, v[u].z, acc.z);
+            acc.w = fmaf(wgt, v[u].w, acc.w);
+        }
     }
     red_o[warp][lane] = acc;
     if (lane == 0) red_l[warp] = lsum;

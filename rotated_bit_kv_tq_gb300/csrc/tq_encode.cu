@@ -206,8 +206,11 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
     }
 }
 
+// blockIdx.y selects the cache: one launch can encode the K and the V rows of a step.
 template <int TYPE>
-__global__ void __launch_bounds__(kThreads, 3) encode_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3) encode_kernel(const EncodeParams p0,
+                                                             const EncodeParams p1) {
+    const EncodeParams &p = blockIdx.y ? p1 : p0;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem<TYPE> &sm = *reinterpret_cast<EncodeSmem<TYPE> *>(smem_raw);
     constexpr int B = block_bytes(TYPE);
@@ -266,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 3) encode_kernel(const EncodeParams 
 }
 
 template <int TYPE>
-tq_status launch_encode_t(const EncodeParams &p, cudaStream_t stream) {
+tq_status launch_encode_t(const EncodeParams &p0, const EncodeParams &p1, int n_caches,
+                          cudaStream_t stream) {
     const size_t smem = sizeof(EncodeSmem<TYPE>);
     if (cudaFuncSetAttribute(encode_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
@@ -276,16 +280,15 @@ tq_status launch_encode_t(const EncodeParams &p, cudaStream_t stream) {
                                                       smem) != cudaSuccess)
         return TQ_ERR_CUDA;
     if (per_sm < 1) per_sm = 1;
-    const int64_t grid = min64(p.n_tiles, (int64_t)device_sm_count() * per_sm);
-    encode_kernel<TYPE><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+    const int64_t slots = max64(1, (int64_t)device_sm_count() * per_sm / n_caches);
+    const int64_t grid = min64(max64(p0.n_tiles, p1.n_tiles), slots);
+    encode_kernel<TYPE><<<dim3((unsigned)grid, (unsigned)n_caches), kThreads, smem, stream>>>(p0, p1);
     return check_cuda(cudaGetLastError());
 }
 
-}  // namespace
-
-tq_status launch_encode(const tq_cache &dst, const void *src, int64_t n_tokens, int64_t stride,
-                        const int32_t *seq_ids, const int32_t *positions, int32_t seq_id,
-                        int64_t pos0, cudaStream_t stream) {
+EncodeParams make_params(const tq_cache &dst, const void *src, int64_t n_tokens, int64_t stride,
+                         const int32_t *seq_ids, const int32_t *positions, int32_t seq_id,
+                         int64_t pos0) {
     EncodeParams p;
     p.dst = make_view(dst);
     p.src = static_cast<const __half *>(src);
@@ -302,8 +305,33 @@ tq_status launch_encode(const tq_cache &dst, const void *src, int64_t n_tokens, 
     p.row_bytes = p.dst.row_bytes;
     p.cpr_magic = div_magic((uint32_t)(p.row_bytes / 16 > 0 ? p.row_bytes / 16 : 1));
     p.hpr_magic = div_magic((uint32_t)(p.row_bytes / 2));
-    return dst.type == TQ_TURBO3 ? launch_encode_t<TQ_TURBO3>(p, stream)
-                                 : launch_encode_t<TQ_TURBO2>(p, stream);
+    return p;
+}
+
+}  // namespace
+
+tq_status launch_encode(const tq_cache &dst, const void *src, int64_t n_tokens, int64_t stride,
+                        const int32_t *seq_ids, const int32_t *positions, int32_t seq_id,
+                        int64_t pos0, cudaStream_t stream) {
+    const EncodeParams p = make_params(dst, src, n_tokens, stride, seq_ids, positions, seq_id, pos0);
+    return dst.type == TQ_TURBO3 ? launch_encode_t<TQ_TURBO3>(p, p, 1, stream)
+                                 : launch_encode_t<TQ_TURBO2>(p, p, 1, stream);
+}
+
+tq_status launch_encode_kv(const tq_cache &k, const tq_cache &v, const void *k_src,
+                           const void *v_src, int64_t n_tokens, int64_t k_stride,
+                           int64_t v_stride, const int32_t *seq_ids, const int32_t *positions,
+                           int32_t seq_id, int64_t pos0, cudaStream_t stream) {
+    const EncodeParams pk = make_params(k, k_src, n_tokens, k_stride, seq_ids, positions, seq_id, pos0);
+    const EncodeParams pv = make_params(v, v_src, n_tokens, v_stride, seq_ids, positions, seq_id, pos0);
+    if (k.type != v.type) {   // one template per type: two launches
+        tq_status st = launch_encode(k, k_src, n_tokens, k_stride, seq_ids, positions, seq_id,
+                                     pos0, stream);
+        if (st != TQ_OK) return st;
+        return launch_encode(v, v_src, n_tokens, v_stride, seq_ids, positions, seq_id, pos0, stream);
+    }
+    return k.type == TQ_TURBO3 ? launch_encode_t<TQ_TURBO3>(pk, pv, 2, stream)
+                               : launch_encode_t<TQ_TURBO2>(pk, pv, 2, stream);
 }
 
 }  // namespace tq

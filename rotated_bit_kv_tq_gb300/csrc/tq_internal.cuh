@@ -102,6 +102,10 @@ tq_status validate_cache(const tq_cache *c);
 tq_status launch_encode(const tq_cache &dst, const void *src, int64_t n_tokens, int64_t stride,
                         const int32_t *seq_ids, const int32_t *positions, int32_t seq_id,
                         int64_t pos0, cudaStream_t stream);
+tq_status launch_encode_kv(const tq_cache &k, const tq_cache &v, const void *k_src,
+                           const void *v_src, int64_t n_tokens, int64_t k_stride,
+                           int64_t v_stride, const int32_t *seq_ids, const int32_t *positions,
+                           int32_t seq_id, int64_t pos0, cudaStream_t stream);
 tq_status launch_decode(const tq_cache &src, int32_t seq_id, int64_t pos0, int64_t n_tokens,
                         float *dst, cudaStream_t stream);
 size_t attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max_seq_len,

@@ -318,3 +318,22 @@ def test_qwen14b_bytes_freed_and_mse(tq):
             xf = x.float().reshape(T, w.n_kv_heads, w.head_dim)
             nmse = float(((xf - xh) ** 2).sum() / (xf ** 2).sum())
             assert mse_lo < nmse < mse_hi, (tt, kind, nmse)
+
+
+@pytest.mark.parametrize("tk,tv", [(3, 3), (2, 2), (3, 2)])
+def test_encode_kv_one_launch_bit_exact(tq, tk, tv):
+    """tq_encode_kv writes K and V rows exactly as two tq_encode calls (and the oracle) do,
+    for whole prefills and for one-token appends at device positions."""
+    w = synth.LLAMA3_8B_32K
+    n = 300
+    k = _kv(w, 1, "K", n)
+    v = _kv(w, 1, "V", n)
+    kc = tq.KVCache(tk, w.n_kv_heads, w.head_dim, capacity_tokens=n + 1)
+    vc = tq.KVCache(tv, w.n_kv_heads, w.head_dim, capacity_tokens=n + 1)
+    tq.encode_kv(kc, vc, torch.from_numpy(k).to(DEV), torch.from_numpy(v).to(DEV))
+    kn, vn = _kv(w, 1, "K", 1, t0=n), _kv(w, 1, "V", 1, t0=n)
+    pos = torch.tensor([n], dtype=torch.int32, device=DEV)
+    tq.encode_kv(kc, vc, torch.from_numpy(kn).to(DEV), torch.from_numpy(vn).to(DEV), positions=pos)
+    assert tq.device_status() == 0
+    assert np.array_equal(_rows_from(kc, n + 1), oracle.encode_rows(tk, np.concatenate([k, kn]), w.n_kv_heads, w.head_dim))
+    assert np.array_equal(_rows_from(vc, n + 1), oracle.encode_rows(tv, np.concatenate([v, vn]), w.n_kv_heads, w.head_dim))
