@@ -42,6 +42,15 @@ constexpr uint32_t kWaitLimit = 1u << 26;  // bounded mbarrier wait (tens of ms)
 __host__ __device__ constexpr int ctas_per_sm(int nb) { return nb == 1 ? 2 : 1; }
 constexpr size_t kSmemBudget = 220 * 1024;   // per SM
 
+// Rotated queries in shared memory, in MMA-fragment order: head h, block b, k-step j and
+// lane quarter q4 hold the four values 32 q4 + 4j .. +3 at halfs h*QS + 128 b + 16 j + 4 q4.
+// QS = 128 nb + 16 puts consecutive heads 8 banks apart, so the 8-byte B-fragment loads of
+// four heads x four quarters cover all 32 banks once (eight heads: two wavefronts).
+__host__ __device__ constexpr int q_stride(int nb) { return 128 * nb + 16; }
+inline size_t q_bytes(int n_q_heads, int nb) {
+    return ((size_t)n_q_heads * q_stride(nb) * 2 + 127) & ~size_t(127);
+}
+
 struct MmaParams {
     CacheView kc, vc;
     const __half *q;
@@ -56,6 +65,14 @@ struct MmaParams {
     int32_t stages;
     int32_t stage_bytes;
     int32_t cpart_offset;   // bytes from the first stage to this CTA's partial rows
+    // 2, 4, 2^16, 2^30, 2^31: shift amounts as multipliers passed at run time, so that the
+    // selector shifts compile to integer multiply-adds (FMA pipe) instead of ALU shifts
+    uint32_t mul2, mul4, hi16, hi30, hi31;
+};
+
+// Run-time multipliers of one launch (see MmaParams).
+struct Shifts {
+    uint32_t mul2, mul4, hi16, hi30, hi31;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -129,10 +146,11 @@ struct HalfTables {
 // low-plane word is W, high-plane bit 4k+p of V (layout of tq.h).  Left shifts are
 // integer multiplies so that they issue on the FMA pipe, not the half-rate ALU pipe.
 template <int TYPE>
-__device__ __forceinline__ uint32_t sel8(uint32_t W, uint32_t V, int r, int p) {
-    uint32_t x = (r ? (W >> 2) : W) & 0x33333333u;
+__device__ __forceinline__ uint32_t sel8(uint32_t W, uint32_t V, int r, int p, const Shifts &k) {
+    uint32_t x = (r ? __umulhi(W, k.hi30) : W) & 0x33333333u;      // W >> 2 for r = 1
     if (TYPE == TQ_TURBO3) {
-        const uint32_t hv = p == 0 ? V * 4u : p == 1 ? V * 2u : p == 2 ? V : (V >> 1);
+        // bit 4k+p of V moves to 4k+2: V << 2, V << 1, V, V >> 1
+        const uint32_t hv = p == 0 ? V * k.mul4 : p == 1 ? V * k.mul2 : p == 2 ? V : __umulhi(V, k.hi31);
         x |= hv & 0x44444444u;
     }
     return x;
@@ -146,10 +164,11 @@ __device__ __forceinline__ void lookup4(const HalfTables &t, uint32_t sel, uint3
 }
 
 // The 4 fp16x2 pairs (values 8r+2i, 8r+2i+1 for i = 0..3) of one selector.
-__device__ __forceinline__ void pairs8(const HalfTables &t, uint32_t sel, uint32_t (&o)[4]) {
+__device__ __forceinline__ void pairs8(const HalfTables &t, uint32_t sel, uint32_t hi16,
+                                       uint32_t (&o)[4]) {
     uint32_t L, H, Lh, Hh;
     lookup4(t, sel, L, H);
-    lookup4(t, __umulhi(sel, 0x10000u), Lh, Hh);   // sel >> 16 on the FMA pipe
+    lookup4(t, __umulhi(sel, hi16), Lh, Hh);   // sel >> 16 on the FMA pipe
     o[0] = prmt(L, H, 0x5140);
     o[1] = prmt(L, H, 0x7362);
     o[2] = prmt(Lh, Hh, 0x5140);
@@ -163,17 +182,18 @@ template <int TYPE>
 struct Quarter {
     uint32_t W0, W1, V;
 };
+// `row` is a 16-byte aligned packed row in shared memory; ow / ov are the word-aligned
+// byte offsets (within the row) of the quarter's low-plane and high-plane words.
 template <int TYPE>
-__device__ __forceinline__ Quarter<TYPE> load_quarter(const uint8_t *blk, int q4, uint32_t sh) {
+__device__ __forceinline__ Quarter<TYPE> load_quarter(const uint8_t *row, int ow, int ov,
+                                                      uint32_t sh) {
     Quarter<TYPE> r;
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(
-        reinterpret_cast<uintptr_t>(blk + 2 + 8 * q4) & ~uintptr_t(3));
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(row + ow);
     const uint32_t a = w[0], b = w[1], c = w[2];
     r.W0 = __funnelshift_r(a, b, sh);
     r.W1 = __funnelshift_r(b, c, sh);
     if (TYPE == TQ_TURBO3) {
-        const uint32_t *v = reinterpret_cast<const uint32_t *>(
-            reinterpret_cast<uintptr_t>(blk + 34 + 4 * q4) & ~uintptr_t(3));
+        const uint32_t *v = reinterpret_cast<const uint32_t *>(row + ov);
         r.V = __funnelshift_r(v[0], v[1], sh);
     } else {
         r.V = 0u;
@@ -184,8 +204,9 @@ __device__ __forceinline__ Quarter<TYPE> load_quarter(const uint8_t *blk, int q4
 // Group (ww, r) of a quarter: the 4 pairs 8ww + 4r + {0..3}.
 template <int TYPE>
 __device__ __forceinline__ void group_pairs(const Quarter<TYPE> &qw, int ww, int r,
-                                            const HalfTables &t, uint32_t (&o)[4]) {
-    pairs8(t, sel8<TYPE>(ww ? qw.W1 : qw.W0, qw.V, r, 2 * ww + r), o);
+                                            const HalfTables &t, const Shifts &k,
+                                            uint32_t (&o)[4]) {
+    pairs8(t, sel8<TYPE>(ww ? qw.W1 : qw.W0, qw.V, r, 2 * ww + r, k), k.hi16, o);
 }
 
 // Rotate the query of one (head, block) pair held by a warp, four values per lane
@@ -260,8 +281,9 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
     const int TT = p.tile_tokens;
     const int seq = blockIdx.y, split = blockIdx.x;
 
-    __half *qh = reinterpret_cast<__half *>(smem);                          // [Hq][D]
-    const size_t qbytes = ((size_t)Hq * D * 2 + 127) & ~size_t(127);
+    constexpr int QS = q_stride(NB);
+    __half *qh = reinterpret_cast<__half *>(smem);                          // [Hq][QS]
+    const size_t qbytes = ((size_t)Hq * QS * 2 + 127) & ~size_t(127);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + qbytes);          // [stages]
     uint64_t *empty = full + 4;                                            // [stages]
     uint8_t *stage0 = smem + qbytes + 128;
@@ -294,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
         uint2 o;
         o.x = pack_half2(v[0] * p.score_scale, v[1] * p.score_scale);
         o.y = pack_half2(v[2] * p.score_scale, v[3] * p.score_scale);
-        *reinterpret_cast<uint2 *>(qh + h * D + b * kBlock + 4 * lane) = o;
+        // lane = 8 q4 + j holds values 4 lane .. 4 lane + 3 = 32 q4 + 4 j ..
+        *reinterpret_cast<uint2 *>(qh + h * QS + b * kBlock + 16 * (lane & 7) + 4 * (lane >> 3)) = o;
     }
     __syncthreads();
 
@@ -324,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
         // B fragments of the rotated query (head n = g8 of KV head g, values 32q4 + 4j + e)
         // are read from shared memory at each use: one 8-byte load per k-step.
         const bool qv = g8 < G;
-        const __half *qrow = qh + (g * G + (qv ? g8 : 0)) * D + 32 * q4;
+        const __half *qrow = qh + (g * G + (qv ? g8 : 0)) * QS + 4 * q4;
         auto bq = [&](int b, int j) -> uint2 {
-            const uint2 v = *reinterpret_cast<const uint2 *>(qrow + b * kBlock + 4 * j);
+            const uint2 v = *reinterpret_cast<const uint2 *>(qrow + b * kBlock + 16 * j);
             return qv ? v : make_uint2(0u, 0u);
         };
         HalfTables tk, tv;
@@ -346,13 +369,21 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
             tk = {lk[0], lk[1], hk[0], hk[1]};
             tv = {lv[0], lv[1], hv[0], hv[1]};
         }
-        // word alignment of this warp's blocks (same for every row: rows are 16-byte multiples)
+        // word alignment of this warp's blocks (same for every row: rows are 16-byte
+        // multiples) and the word-aligned offsets of this lane's quarter within a row
         uint32_t shk[NB], shv[NB];
+        int owk[NB], ovk[NB], owv[NB], ovv[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            shk[b] = (uint32_t)(((g * NB + b) * BK + 2) & 3) * 8u;
-            shv[b] = (uint32_t)(((g * NB + b) * BV + 2) & 3) * 8u;
+            const int bk = (g * NB + b) * BK, bv = (g * NB + b) * BV;
+            shk[b] = (uint32_t)((bk + 2) & 3) * 8u;
+            shv[b] = (uint32_t)((bv + 2) & 3) * 8u;
+            owk[b] = (bk + 2 + 8 * q4) & ~3;
+            ovk[b] = (bk + 34 + 4 * q4) & ~3;
+            owv[b] = (bv + 2 + 8 * q4) & ~3;
+            ovv[b] = (bv + 34 + 4 * q4) & ~3;
         }
+        const Shifts ks = {p.mul2, p.mul4, p.hi16, p.hi30, p.hi31};
         const int wr0 = sub * kWarpTokens;   // this warp's first row in every tile
 
         for (int i = 0; i < n_tiles; ++i) {
@@ -381,10 +412,9 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
                     for (int b = 0; b < NB; ++b)
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
-                            const uint8_t *bk =
-                                Kt + (size_t)(hr0 + 16 * mt + g8 + 8 * t) * Rk + (g * NB + b) * BK;
-                            kq[mt][b][t] = load_quarter<TK>(bk, q4, shk[b]);
-                            kn[mt][b][t] = ld_norm(bk);
+                            const uint8_t *rk = Kt + (size_t)(hr0 + 16 * mt + g8 + 8 * t) * Rk;
+                            kq[mt][b][t] = load_quarter<TK>(rk, owk[b], ovk[b], shk[b]);
+                            kn[mt][b][t] = ld_norm(rk + (g * NB + b) * BK);
                         }
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
@@ -404,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
 #pragma unroll
                             for (int r = 0; r < 2; ++r) {
                                 uint32_t xa[4], xb[4];
-                                group_pairs<TK>(qa, ww, r, tk, xa);
-                                group_pairs<TK>(qb, ww, r, tk, xb);
+                                group_pairs<TK>(qa, ww, r, tk, ks, xa);
+                                group_pairs<TK>(qb, ww, r, tk, ks, xb);
                                 const int j = 4 * ww + 2 * r;
                                 const uint2 q0 = bq(b, j), q1 = bq(b, j + 1);
                                 mma16816(acc[0], xa[0], xb[0], xa[1], xb[1], q0.x, q0.y);
@@ -478,10 +508,10 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
                             const int row = hr0 + 16 * mt + g8 + 8 * t;
-                            const uint8_t *bv = Vt + (size_t)row * Rv + (g * NB + b) * BV;
-                            vq[mt][b][t] = load_quarter<TV>(bv, q4, shv[b]);
+                            const uint8_t *rv = Vt + (size_t)row * Rv;
+                            vq[mt][b][t] = load_quarter<TV>(rv, owv[b], ovv[b], shv[b]);
                             // masked rows may hold stale bytes: their weight is forced to 0
-                            vn[mt][b][t] = row < nt ? ld_norm(bv) : 0.f;
+                            vn[mt][b][t] = row < nt ? ld_norm(rv + (g * NB + b) * BV) : 0.f;
                         }
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
@@ -497,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
 #pragma unroll
                             for (int r = 0; r < 2; ++r) {
                                 uint32_t ya[4], yb[4];
-                                group_pairs<TV>(qa, ww, r, tv, ya);
-                                group_pairs<TV>(qb, ww, r, tv, yb);
+                                group_pairs<TV>(qa, ww, r, tv, ks, ya);
+                                group_pairs<TV>(qb, ww, r, tv, ks, yb);
                                 const int j = 4 * ww + 2 * r;   // m-tiles j, j+1: pairs 2j..2j+3
                                 mma16816(oacc[b][j], movtrans(ya[0]), movtrans(ya[1]),
                                          movtrans(yb[0]), movtrans(yb[1]), b0, b1);
@@ -665,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
 
 template <int TK, int TV, int NB>
 tq_status launch_t(const MmaParams &p, int n_seqs, cudaStream_t stream) {
-    const size_t qbytes = ((size_t)p.n_q_heads * p.head_dim * 2 + 127) & ~size_t(127);
+    const size_t qbytes = q_bytes(p.n_q_heads, NB);
     const size_t smem = qbytes + 128 + (size_t)p.stages * p.stage_bytes;
     if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -708,7 +738,7 @@ bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
     const int TT = kWarpTokens * (kConsumers / hkv);
     if (k.page_tokens && k.page_tokens % 16) return false;
     if (v.page_tokens && v.page_tokens % 16) return false;
-    const size_t qbytes = ((size_t)n_q_heads * k.head_dim * 2 + 127) & ~size_t(127);
+    const size_t qbytes = q_bytes(n_q_heads, nb);
     return qbytes + 128 + 2 * stage_bytes_for(TT, rk, rv) <= kSmemBudget / ctas_per_sm(nb);
 }
 
@@ -731,10 +761,15 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     p.tokens_per_split = tokens_per_split;
     p.wph = kConsumers / k.n_kv_heads;
     p.tile_tokens = kWarpTokens * p.wph;
+    p.mul2 = 2u;
+    p.mul4 = 4u;
+    p.hi16 = 1u << 16;
+    p.hi30 = 1u << 30;
+    p.hi31 = 1u << 31;
     const size_t stage = stage_bytes_for(p.tile_tokens, p.kc.row_bytes, p.vc.row_bytes);
     p.stage_bytes = (int)stage;
-    const size_t qbytes = ((size_t)n_q_heads * k.head_dim * 2 + 127) & ~size_t(127);
     const int nb = k.head_dim / kBlock;
+    const size_t qbytes = q_bytes(n_q_heads, nb);
     p.stages = (int)std::min<size_t>(4, (kSmemBudget / ctas_per_sm(nb) - qbytes - 128) / stage);
     if (p.stages < 2) return TQ_ERR_UNSUPPORTED;
     if (n_splits % kClusterSplits) return TQ_ERR_UNSUPPORTED;
