@@ -304,33 +304,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
 // Warps take splits round-robin, lanes take four coordinates each (float4 loads of the
 // partial rows), the eight warp sums meet in shared memory, and one warp applies the
 // inverse FWHT with shuffles.
+// Rows of split partials each warp keeps in flight at once.
+constexpr int kMergeRows = 24;
+
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     // launched as a programmatic dependent of the partial kernel: wait for its results
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ float red_m[8], red_l[8];
     __shared__ float4 red_o[8][32];
     const int h = blockIdx.x, seq = blockIdx.y, b = blockIdx.z, D = p.head_dim;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *base = p.part + ((int64_t)seq * p.n_splits * p.n_q_heads + h) * part_stride(D);
     const int64_t sstride = (int64_t)p.n_q_heads * part_stride(D);
-    // global maximum of the split maxima
-    float mx = -INFINITY;
-    for (int s = tid; s < p.n_splits; s += 256) mx = fmaxf(mx, base[s * sstride + D]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red_m[warp] = mx;
-    __syncthreads();
-    mx = red_m[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red_m[w]);
-    // weighted sums: warp w handles splits w, w+8, ...; four rows in flight at a time
+    // One pass: warp w takes splits w, w + 8, ...; all rows of a round are loaded before
+    // any is used, and the warp's running maximum rescales what it has summed so far.
+    float M = -INFINITY, lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lsum = 0.f;
-    for (int s0 = warp; s0 < p.n_splits; s0 += 32) {
-        float2 ml[4];
-        float4 v[4];
+    for (int s0 = warp; s0 < p.n_splits; s0 += 8 * kMergeRows) {
+        float2 ml[kMergeRows];
+        float4 v[kMergeRows];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kMergeRows; ++u) {
             const int s = s0 + 8 * u;
             if (s < p.n_splits) {
                 const float *row = base + s * sstride;
@@ -341,9 +336,21 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
                 v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
+        float mc = M;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float wgt = (ml[u].x == -INFINITY) ? 0.f : __expf(ml[u].x - mx);
+        for (int u = 0; u < kMergeRows; ++u) mc = fmaxf(mc, ml[u].x);
+        if (mc != M) {   // new maximum: rescale (M = -inf means nothing was summed yet)
+            const float r = M == -INFINITY ? 0.f : __expf(M - mc);
+            lsum *= r;
+            acc.x *= r;
+            acc.y *= r;
+            acc.z *= r;
+            acc.w *= r;
+            M = mc;
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeRows; ++u) {
+            const float wgt = (ml[u].x == -INFINITY) ? 0.f : __expf(ml[u].x - M);
             lsum += wgt * ml[u].y;
             acc.x = fmaf(wgt, v[u].x, acc.x);
             acc.y = fmaf(wgt, v[u].y, acc.y);
@@ -352,19 +359,27 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
         }
     }
     red_o[warp][lane] = acc;
-    if (lane == 0) red_l[warp] = lsum;
+    if (lane == 0) {
+        red_m[warp] = M;
+        red_l[warp] = lsum;
+    }
     __syncthreads();
     if (warp != 0) return;
+    float mx = red_m[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red_m[w]);
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     float L = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
+        const float mw = red_m[w];
+        const float wgt = mw == -INFINITY ? 0.f : __expf(mw - mx);
         const float4 a = red_o[w][lane];
-        v[0] += a.x;
-        v[1] += a.y;
-        v[2] += a.z;
-        v[3] += a.w;
-        L += red_l[w];
+        v[0] = fmaf(wgt, a.x, v[0]);
+        v[1] = fmaf(wgt, a.y, v[1]);
+        v[2] = fmaf(wgt, a.z, v[2]);
+        v[3] = fmaf(wgt, a.w, v[3]);
+        L = fmaf(wgt, red_l[w], L);
     }
     const float inv = L > 0.f ? kInvSqrt128 / L : 0.f;
     // inverse rotation (1/sqrt(128)) W o_b, values 4*lane .. 4*lane+3
@@ -381,16 +396,8 @@ size_t partial_smem(const AttnParams &p) {
 }
 
 tq_status launch_merge(const AttnParams &p, int n_seqs, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_q_heads, n_seqs, p.nb);
-    cfg.blockDim = dim3(256);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return check_cuda(cudaLaunchKernelEx(&cfg, attn_merge_kernel, p));
+    PdlConfig lc(dim3(p.n_q_heads, n_seqs, p.nb), dim3(256), 0, stream);
+    return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_merge_kernel, p));
 }
 
 template <int TK, int TV>

@@ -288,6 +288,18 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
     uint64_t *empty = full + 4;                                            // [stages]
     uint8_t *stage0 = smem + qbytes + 128;
 
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), kConsumers);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    // everything above touches only shared memory; inputs may come from the kernel
+    // launched before this one
+    pdl_wait();
+    pdl_launch_dependents();
+
     int64_t len = p.seq_lens[seq];
     if (len < 0 || len > p.max_len) {
         if (tid == 0) record_error(TQ_ERR_OUT_OF_RANGE);
@@ -296,14 +308,6 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
     const int64_t t_begin = (int64_t)split * p.tokens_per_split;
     const int64_t t_end = min64(len, t_begin + p.tokens_per_split);
     const int n_tiles = t_end > t_begin ? (int)((t_end - t_begin + TT - 1) / TT) : 0;
-
-    if (tid == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), kConsumers);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
     // ---- rotate q once per call: qh = fp16(W q_b * scale * log2(e) / sqrt(128))
     for (int hb = warp; hb < Hq * NB; hb += kConsumers) {
         const int h = hb / NB, b = hb - h * NB;
@@ -687,8 +691,6 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
             }
         }
     }
-    // let the merge kernel start its launch; it waits for this grid to finish anyway
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // nobody leaves while a peer may still read its shared memory
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
@@ -700,19 +702,13 @@ tq_status launch_t(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return TQ_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_splits, n_seqs);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kClusterSplits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return check_cuda(cudaLaunchKernelEx(&cfg, attn_mma_kernel<TK, TV, NB>, p));
+    PdlConfig lc(dim3(p.n_splits, n_seqs), dim3(kThreads), smem, stream);
+    lc.attrs[1].id = cudaLaunchAttributeClusterDimension;
+    lc.attrs[1].val.clusterDim.x = kClusterSplits;
+    lc.attrs[1].val.clusterDim.y = 1;
+    lc.attrs[1].val.clusterDim.z = 1;
+    lc.cfg.numAttrs = 2;
+    return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_mma_kernel<TK, TV, NB>, p));
 }
 
 template <int NB>

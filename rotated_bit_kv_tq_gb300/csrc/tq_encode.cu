@@ -214,6 +214,8 @@ __global__ void __launch_bounds__(kThreads, 3) encode_kernel(const EncodeParams 
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem<TYPE> &sm = *reinterpret_cast<EncodeSmem<TYPE> *>(smem_raw);
     constexpr int B = block_bytes(TYPE);
+    pdl_wait();
+    pdl_launch_dependents();
 
     int64_t tile = blockIdx.x;
     if (tile < p.n_tiles) load_tile(p, tile, sm.in[0]);
@@ -282,8 +284,127 @@ tq_status launch_encode_t(const EncodeParams &p0, const EncodeParams &p1, int n_
     if (per_sm < 1) per_sm = 1;
     const int64_t slots = max64(1, (int64_t)device_sm_count() * per_sm / n_caches);
     const int64_t grid = min64(max64(p0.n_tiles, p1.n_tiles), slots);
-    encode_kernel<TYPE><<<dim3((unsigned)grid, (unsigned)n_caches), kThreads, smem, stream>>>(p0, p1);
-    return check_cuda(cudaGetLastError());
+    PdlConfig lc(dim3((unsigned)grid, (unsigned)n_caches), dim3(kThreads), smem, stream);
+    return check_cuda(cudaLaunchKernelEx(&lc.cfg, encode_kernel<TYPE>, p0, p1));
+}
+
+// ------------------------------------------------------------------ small appends
+// A decode step appends one token (or one per sequence): a few hundred blocks at most,
+// too few to fill the GPU with one block per thread.  Here a warp encodes one block, four
+// values per lane, so the latency of a block is that of ~200 instructions.  The operation
+// order is the one of encode_one: the norm tree pairs element i with i + len/2 (lanes
+// xor 16, 8, 4, 2, 1, then in-lane), butterflies run h = 1, 2 (in-lane) and 4 .. 64
+// (lanes xor 1 .. 16), every operation rounded separately, so the codes and norms are
+// the same bits.
+constexpr int kWarpPathWarps = 8;               // warps (blocks) per CTA
+constexpr int64_t kWarpPathMaxBlocks = 4096;    // larger calls use encode_kernel
+
+template <int TYPE>
+__global__ void __launch_bounds__(32 * kWarpPathWarps) encode_warp_kernel(const EncodeParams p0,
+                                                                          const EncodeParams p1) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const EncodeParams &p = blockIdx.y ? p1 : p0;
+    const Codebook &cb = c_codebook[cb_index(TYPE)];
+    constexpr int L = 1 << TYPE, B = block_bytes(TYPE);
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpPathWarps + (threadIdx.x >> 5);
+    if (gw >= p.n_tokens * p.bpr) return;   // whole warp
+    const int64_t t = gw / p.bpr;
+    const int jb = (int)(gw - t * p.bpr);
+    // values 4 lane .. 4 lane + 3 of the block
+    const uint2 raw = *reinterpret_cast<const uint2 *>(p.src + t * p.stride + jb * kBlock + 4 * lane);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+    float x[4] = {f01.x, f01.y, f23.x, f23.y};
+    // norm
+    float sq[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sq[e] = __fmul_rn(x[e], x[e]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sq[e] = __fadd_rn(sq[e], __shfl_xor_sync(0xffffffffu, sq[e], off));
+    const float n = __fsqrt_rn(__fadd_rn(__fadd_rn(sq[0], sq[2]), __fadd_rn(sq[1], sq[3])));
+    const uint16_t norm16 = __half_as_ushort(__float2half_rn(fminf(n, 65504.0f)));
+    const float k = n > 0.0f ? __fdiv_rn(kInvSqrt128, n) : 0.0f;
+    // butterflies
+    {
+        const float a0 = __fadd_rn(x[0], x[1]), a1 = __fsub_rn(x[0], x[1]);
+        const float a2 = __fadd_rn(x[2], x[3]), a3 = __fsub_rn(x[2], x[3]);
+        x[0] = __fadd_rn(a0, a2);
+        x[2] = __fsub_rn(a0, a2);
+        x[1] = __fadd_rn(a1, a3);
+        x[3] = __fsub_rn(a1, a3);
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = lane & m;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+            x[e] = upper ? __fsub_rn(o, x[e]) : __fadd_rn(x[e], o);
+        }
+    }
+    // sign-magnitude quantiser: m = #{positive thresholds strictly below |y|},
+    // code = signbit(y) ? L/2 - 1 - m : L/2 + m; pack into this lane's share of the words
+    uint32_t wlo = 0, whi = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float y = __fmul_rn(x[e], k);
+        const float a = fabsf(y);
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = L / 2; j <= L - 2; ++j) m += a > cb.threshold[j] ? 1u : 0u;
+        const uint32_t c = signbit(y) ? (uint32_t)(L / 2 - 1) - m : (uint32_t)(L / 2) + m;
+        const int jl = 4 * (lane & 3) + e;          // value index within its 16-value word
+        wlo |= (c & 3u) << (4 * (jl & 7) + 2 * (jl >> 3));
+        if (TYPE == TQ_TURBO3) {
+            const int jh = 4 * (lane & 7) + e;      // value index within its 32-value word
+            whi |= (c >> 2) << (4 * (jh & 7) + (jh >> 3));
+        }
+    }
+    wlo |= __shfl_xor_sync(0xffffffffu, wlo, 1);
+    wlo |= __shfl_xor_sync(0xffffffffu, wlo, 2);
+    if (TYPE == TQ_TURBO3) {
+        whi |= __shfl_xor_sync(0xffffffffu, whi, 1);
+        whi |= __shfl_xor_sync(0xffffffffu, whi, 2);
+        whi |= __shfl_xor_sync(0xffffffffu, whi, 4);
+    }
+    const int64_t seq = p.seq_ids ? (int64_t)p.seq_ids[t] : (int64_t)p.seq_id;
+    const int64_t pos = p.positions ? (int64_t)p.positions[t] : p.pos0 + t;
+    uint8_t *row = nullptr;
+    if (lane == 0) row = row_ptr(p.dst, seq, pos);   // records an out-of-range row once
+    row = reinterpret_cast<uint8_t *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(row), 0));
+    if (!row) return;
+    uint16_t *o = reinterpret_cast<uint16_t *>(row + (int64_t)jb * B);   // 2-byte aligned
+    if (lane == 0) o[0] = norm16;
+    if ((lane & 3) == 0) {
+        o[1 + 2 * (lane >> 2)] = (uint16_t)(wlo & 0xffffu);
+        o[2 + 2 * (lane >> 2)] = (uint16_t)(wlo >> 16);
+    }
+    if (TYPE == TQ_TURBO3 && (lane & 7) == 0) {
+        o[17 + 2 * (lane >> 3)] = (uint16_t)(whi & 0xffffu);
+        o[18 + 2 * (lane >> 3)] = (uint16_t)(whi >> 16);
+    }
+}
+
+template <int TYPE>
+tq_status launch_encode_warp_t(const EncodeParams &p0, const EncodeParams &p1, int n_caches,
+                               cudaStream_t stream) {
+    const int64_t blocks = max64(p0.n_tokens * p0.bpr, p1.n_tokens * p1.bpr);
+    const int64_t grid = (blocks + kWarpPathWarps - 1) / kWarpPathWarps;
+    PdlConfig lc(dim3((unsigned)grid, (unsigned)n_caches), dim3(32 * kWarpPathWarps), 0, stream);
+    return check_cuda(cudaLaunchKernelEx(&lc.cfg, encode_warp_kernel<TYPE>, p0, p1));
+}
+
+// One launch for one or two caches of the same type: small calls take the warp path.
+template <int TYPE>
+tq_status launch_encode_any(const EncodeParams &p0, const EncodeParams &p1, int n_caches,
+                            cudaStream_t stream) {
+    const int64_t blocks = max64(p0.n_tokens * p0.bpr, p1.n_tokens * p1.bpr);
+    return blocks <= kWarpPathMaxBlocks ? launch_encode_warp_t<TYPE>(p0, p1, n_caches, stream)
+                                        : launch_encode_t<TYPE>(p0, p1, n_caches, stream);
 }
 
 EncodeParams make_params(const tq_cache &dst, const void *src, int64_t n_tokens, int64_t stride,
@@ -314,8 +435,8 @@ tq_status launch_encode(const tq_cache &dst, const void *src, int64_t n_tokens, 
                         const int32_t *seq_ids, const int32_t *positions, int32_t seq_id,
                         int64_t pos0, cudaStream_t stream) {
     const EncodeParams p = make_params(dst, src, n_tokens, stride, seq_ids, positions, seq_id, pos0);
-    return dst.type == TQ_TURBO3 ? launch_encode_t<TQ_TURBO3>(p, p, 1, stream)
-                                 : launch_encode_t<TQ_TURBO2>(p, p, 1, stream);
+    return dst.type == TQ_TURBO3 ? launch_encode_any<TQ_TURBO3>(p, p, 1, stream)
+                                 : launch_encode_any<TQ_TURBO2>(p, p, 1, stream);
 }
 
 tq_status launch_encode_kv(const tq_cache &k, const tq_cache &v, const void *k_src,
@@ -330,8 +451,8 @@ tq_status launch_encode_kv(const tq_cache &k, const tq_cache &v, const void *k_s
         if (st != TQ_OK) return st;
         return launch_encode(v, v_src, n_tokens, v_stride, seq_ids, positions, seq_id, pos0, stream);
     }
-    return k.type == TQ_TURBO3 ? launch_encode_t<TQ_TURBO3>(pk, pv, 2, stream)
-                               : launch_encode_t<TQ_TURBO2>(pk, pv, 2, stream);
+    return k.type == TQ_TURBO3 ? launch_encode_any<TQ_TURBO3>(pk, pv, 2, stream)
+                               : launch_encode_any<TQ_TURBO2>(pk, pv, 2, stream);
 }
 
 }  // namespace tq

@@ -76,6 +76,34 @@ __device__ __forceinline__ uint8_t *row_ptr(const CacheView &c, int64_t seq, int
     }
     return c.base + row * (int64_t)c.row_bytes;
 }
+
+// Programmatic dependent launch.  Kernels launched with the programmatic-serialization
+// attribute may start while the previous kernel in the stream is still running; they call
+// pdl_wait() before their first global-memory access (it returns once that kernel has
+// completed and its writes are visible, and at once for a normal launch).
+// pdl_launch_dependents() lets the next such kernel be scheduled early; it still waits for
+// this one to complete before it touches memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch configuration with the programmatic-serialization attribute set (attrs[0]); a
+// caller may add a second attribute at attrs[1].
+struct PdlConfig {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attrs[2];
+    PdlConfig(dim3 grid, dim3 block, size_t smem, cudaStream_t stream) : cfg(), attrs() {
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 1;
+    }
+};
 #endif  // __CUDACC__
 
 // ------------------------------------------------------------------ codebook tables

@@ -71,10 +71,13 @@ def test_encode_bit_exact(tq, tt, hkv, d, n):
     assert not cache.buffer[n * cache.row_bytes:].any()
 
 
-def test_encode_edge_values(tq):
-    """Zero blocks, single spikes, fp16 extremes, subnormals, norm saturation."""
+@pytest.mark.parametrize("n", [40, 2100])
+def test_encode_edge_values(tq, n):
+    """Zero blocks, single spikes, fp16 extremes, subnormals, norm saturation.  40 tokens
+    (80 blocks) take the warp-per-block encoder of small appends, 2100 tokens (4200
+    blocks) the one-thread-per-block encoder."""
     rng = np.random.default_rng(0)
-    n, hkv, d = 40, 2, 128
+    hkv, d = 2, 128
     x = rng.standard_normal((n, hkv * d)).astype(np.float16)
     x[0] = 0
     x[1] = 0; x[1, 5] = 3.0
