@@ -69,6 +69,7 @@ def _load():
     lib.oracle_decode_rows.argtypes = [i32, P, i64, i32, i32, P, P]
     lib.oracle_dense_attention.argtypes = [P, P, P, i64, i32, i32, i32, dbl, P]
     lib.oracle_attn_decode.argtypes = [i32, i32, P, P, P, i64, i32, i32, i32, dbl, P, P, P]
+    lib.oracle_attn_prefill.argtypes = [i32, i32, P, P, P, i64, i64, i32, i32, i32, dbl, P, P, P]
     _lib = lib
     return lib
 
@@ -204,3 +205,22 @@ def attn_decode(type_k: int, type_v: int, k_rows: np.ndarray, v_rows: np.ndarray
     _load().oracle_attn_decode(type_k, type_v, _ptr(kr), _ptr(vr), _ptr(q), n_tokens, n_q_heads,
                                n_kv_heads, head_dim, float(scale), _ptr(ck), _ptr(cv), _ptr(out))
     return out
+
+
+def attn_prefill(type_k: int, type_v: int, k_rows: np.ndarray, v_rows: np.ndarray,
+                 q_f16: np.ndarray, pos0: int, n_kv_heads: int, head_dim: int,
+                 scale: float) -> np.ndarray:
+    """Causal attention of a prompt chunk: q_f16 [n_q][Hq][D], query j at position pos0 + j
+    over packed rows 0 .. pos0 + j  ->  [n_q][Hq][D] f64."""
+    ck, _ = type_codebook(type_k)
+    cv, _ = type_codebook(type_v)
+    q = np.ascontiguousarray(q_f16).view(np.uint16)
+    n_q, n_q_heads = q.shape[0], q.shape[1]
+    kr = np.ascontiguousarray(k_rows, dtype=np.uint8)
+    vr = np.ascontiguousarray(v_rows, dtype=np.uint8)
+    assert kr.shape[0] >= pos0 + n_q and vr.shape[0] >= pos0 + n_q
+    out = np.zeros((n_q, n_q_heads, head_dim), np.float64)
+    _load().oracle_attn_prefill(type_k, type_v, _ptr(kr), _ptr(vr), _ptr(q), pos0, n_q, n_q_heads,
+                                n_kv_heads, head_dim, float(scale), _ptr(ck), _ptr(cv), _ptr(out))
+    return out
+

@@ -405,3 +405,30 @@ void oracle_attn_decode(int type_k, int type_v, const uint8_t *k_rows,
     oracle_dense_attention(q, k, v, n_tokens, n_q_heads, n_kv_heads, head_dim, scale, out);
     free(k); free(v); free(q);
 }
+
+void oracle_attn_prefill(int type_k, int type_v, const uint8_t *k_rows,
+                         const uint8_t *v_rows, const uint16_t *q_f16, int64_t pos0,
+                         int64_t n_q, int n_q_heads, int n_kv_heads, int head_dim,
+                         double scale, const float *centroids_k, const float *centroids_v,
+                         double *out)
+{
+    const int64_t n_rows = pos0 + n_q;
+    const size_t per_tok = (size_t)n_kv_heads * (size_t)head_dim;
+    const size_t per_q = (size_t)n_q_heads * (size_t)head_dim;
+    size_t n_el = (size_t)(n_rows > 0 ? n_rows : 0) * per_tok;
+    double *k = (double *)malloc((n_el ? n_el : 1) * sizeof(double));
+    double *v = (double *)malloc((n_el ? n_el : 1) * sizeof(double));
+    double *q = (double *)malloc((per_q ? per_q : 1) * sizeof(double));
+    if (!k || !v || !q) { free(k); free(v); free(q); return; }
+    if (n_rows > 0) {
+        oracle_decode_rows(type_k, k_rows, n_rows, n_kv_heads, head_dim, centroids_k, k);
+        oracle_decode_rows(type_v, v_rows, n_rows, n_kv_heads, head_dim, centroids_v, v);
+    }
+    /* query j sees the first pos0 + j + 1 rows */
+    for (int64_t j = 0; j < n_q; ++j) {
+        for (size_t i = 0; i < per_q; ++i) q[i] = oracle_f16_to_f32(q_f16[(size_t)j * per_q + i]);
+        oracle_dense_attention(q, k, v, pos0 + j + 1, n_q_heads, n_kv_heads, head_dim, scale,
+                               out + (size_t)j * per_q);
+    }
+    free(k); free(v); free(q);
+}

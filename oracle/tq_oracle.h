@@ -142,6 +142,20 @@ void oracle_attn_decode(int type_k, int type_v, const uint8_t *k_rows,
                         int head_dim, double scale, const float *centroids_k,
                         const float *centroids_v, double *out);
 
+/* Prompt-chunk (multi-token) attention over a packed cache.  Query token j of the chunk
+ * sits at position pos0 + j and attends to rows 0 .. pos0 + j: the rule of the TinyLLaMA
+ * article, section 7 (the token at position N writes row N and attends to the view of
+ * rows 0..N), applied at every position of the chunk ("llama.cpp に TurboQuant を実装",
+ * "Numbers on real models": prompt processing runs over the compressed cache too).
+ *   q_f16[n_q][n_q_heads][head_dim] (fp16 bits); k_rows / v_rows: pos0 + n_q packed rows;
+ *   out[n_q][n_q_heads][head_dim].
+ * Each query is oracle_dense_attention over its prefix of the dequantised rows. */
+void oracle_attn_prefill(int type_k, int type_v, const uint8_t *k_rows,
+                         const uint8_t *v_rows, const uint16_t *q_f16, int64_t pos0,
+                         int64_t n_q, int n_q_heads, int n_kv_heads, int head_dim,
+                         double scale, const float *centroids_k, const float *centroids_v,
+                         double *out);
+
 #ifdef __cplusplus
 }
 #endif
