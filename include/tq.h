@@ -174,6 +174,29 @@ TQ_API tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void
                          int64_t max_seq_len, float softmax_scale, float *out,
                          void *workspace, size_t ws_bytes, void *stream);
 
+/* Causal attention of a prompt chunk (multi-token / prefill) over the packed caches.
+ * Query token j of the chunk sits at position pos0 + j and attends to rows 0 .. pos0 + j of
+ * cache sequence seq_id: the KV-cache rule of the kenji.blog TinyLLaMA article, section 7
+ * (the token at position N writes row N and attends to the view of rows 0..N), applied at
+ * every position of the chunk.  Prompt processing over the compressed cache is what
+ * "llama.cpp に TurboQuant を実装" measures in "Numbers on real models"; dequantising
+ * inside the Flash-Attention tiles, never forming FP16 K or V in memory, is its roadmap
+ * ("Current implementation and what's next").
+ *   k, v           caches of one layer; same n_kv_heads; head_dim 128 (other head dims
+ *                  return TQ_ERR_UNSUPPORTED); types may differ
+ *   q_f16          device fp16 [n_q][n_q_heads][head_dim], 16-byte aligned
+ *   seq_id         the chunk's sequence; pos0 >= 0 its first position.  The rows of the
+ *                  chunk itself must already be in the caches (encode them first).
+ *   n_q            queries in the chunk; 0 is a no-op
+ *   softmax_scale  score scale; pass 0 for 1/sqrt(head_dim)
+ *   out            device fp32 [n_q][n_q_heads][head_dim], 16-byte aligned
+ * No workspace: one CTA per (block of 128 / G query tokens, KV head) covers all the keys
+ * its queries see.  Rows the device cannot address (page id or position out of range)
+ * are skipped and TQ_ERR_OUT_OF_RANGE is recorded for tq_device_status. */
+TQ_API tq_status tq_attn_prefill(const tq_cache *k, const tq_cache *v, const void *q_f16,
+                                 int32_t seq_id, int64_t pos0, int64_t n_q, int n_q_heads,
+                                 float softmax_scale, float *out, void *stream);
+
 /* tq_attn_decode without a workspace argument, for callers that cannot allocate device
  * memory when they need attention.  Examples are code that runs between the steps of
  * a serving loop whose memory pools are fully reserved at start-up, and embedders whose

@@ -13,7 +13,7 @@ from ._lib import (TQ_BLOCK_VALUES, TQ_TURBO2, TQ_TURBO3, TQError, TqCache, chec
 
 __all__ = ["TQ_TURBO2", "TQ_TURBO3", "TQ_BLOCK_VALUES", "TQError", "TqCache", "KVCache",
            "block_bytes", "row_bytes", "codebook_init", "codebook_get", "encode", "encode_kv", "decode",
-           "attn_workspace_bytes", "attn_decode", "device_status", "load"]
+           "attn_workspace_bytes", "attn_decode", "attn_prefill", "device_status", "load"]
 
 
 def _stream_ptr(stream=None):
@@ -117,6 +117,17 @@ def attn_decode(k: KVCache, v: KVCache, q, seq_lens, max_seq_len: int, out, work
     check(load().tq_attn_decode(ctypes.byref(k.view), ctypes.byref(v.view), _ptr(q), n_seqs,
                                 n_q_heads, _ptr(seq_lens), max_seq_len, softmax_scale, _ptr(out),
                                 _ptr(workspace), ws_bytes, _stream_ptr(stream)), "tq_attn_decode")
+
+
+def attn_prefill(k: KVCache, v: KVCache, q, out, *, pos0: int, seq_id: int = 0,
+                 softmax_scale: float = 0.0, stream=None):
+    """Causal attention of a prompt chunk: q fp16 [n_q, n_q_heads, head_dim], query j at
+    position pos0 + j over cache rows 0 .. pos0 + j of seq_id (its own rows encoded
+    first); out fp32 like q."""
+    n_q, n_q_heads = q.shape[0], q.shape[1]
+    check(load().tq_attn_prefill(ctypes.byref(k.view), ctypes.byref(v.view), _ptr(q), seq_id,
+                                 pos0, n_q, n_q_heads, softmax_scale, _ptr(out),
+                                 _stream_ptr(stream)), "tq_attn_prefill")
 
 
 def device_status(stream=None) -> int:

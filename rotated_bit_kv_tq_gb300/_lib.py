@@ -72,6 +72,10 @@ SIGNATURES = {
                                               ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,
                                               ctypes.c_void_p, ctypes.c_void_p]),
+    "tq_attn_prefill": (ctypes.c_int, [ctypes.POINTER(TqCache), ctypes.POINTER(TqCache),
+                                       ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                       ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                                       ctypes.c_void_p, ctypes.c_void_p]),
     "tq_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }

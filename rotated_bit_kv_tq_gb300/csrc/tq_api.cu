@@ -217,6 +217,29 @@ tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void *q_f16
                        out, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
+tq_status tq_attn_prefill(const tq_cache *k, const tq_cache *v, const void *q_f16,
+                          int32_t seq_id, int64_t pos0, int64_t n_q, int n_q_heads,
+                          float softmax_scale, float *out, void *stream) {
+    tq_status st = validate_cache(k);
+    if (st != TQ_OK) return st;
+    st = validate_cache(v);
+    if (st != TQ_OK) return st;
+    if (k->n_kv_heads != v->n_kv_heads || k->head_dim != v->head_dim)
+        return TQ_ERR_INVALID_ARGUMENT;
+    if (seq_id < 0 || seq_id >= k->n_seqs || seq_id >= v->n_seqs) return TQ_ERR_INVALID_ARGUMENT;
+    if (pos0 < 0 || n_q < 0 || pos0 > (((int64_t)1 << 40) - n_q)) return TQ_ERR_INVALID_ARGUMENT;
+    if (n_q_heads < 1 || n_q_heads % k->n_kv_heads) return TQ_ERR_INVALID_ARGUMENT;
+    if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale)) return TQ_ERR_INVALID_ARGUMENT;
+    if (!prefill_supported(*k, *v, n_q_heads)) return TQ_ERR_UNSUPPORTED;
+    if (n_q == 0) return TQ_OK;   // empty chunk: q and out may be null
+    if (!q_f16 || !out) return TQ_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(q_f16) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+        return TQ_ERR_INVALID_ARGUMENT;
+    if (softmax_scale == 0.0f) softmax_scale = 1.0f / std::sqrt((float)k->head_dim);
+    return launch_prefill(*k, *v, q_f16, seq_id, pos0, n_q, n_q_heads, softmax_scale, out,
+                          static_cast<cudaStream_t>(stream));
+}
+
 tq_status tq_device_status(void *stream, int32_t *status_out) {
     if (!status_out) return TQ_ERR_INVALID_ARGUMENT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
