@@ -8,7 +8,9 @@ hot path over one batch of synthetic input:
   2. 128 decode iterations, each appending one token (tq_encode of K and V, every layer)
      and running tq_attn_decode over the grown context in every layer.
 Metric: decode-attention tokens/s (value) and encode GB/s (encode.gbs), with the
-fraction of the measured HBM peak of the dominant kernel (roofline).
+fraction of the measured HBM peak of the dominant kernel (roofline).  Outside the timed
+step, "prefill" times prompt-chunk attention (tq_attn_prefill) on the last 2,048-token
+chunk of the prompt in every layer, with its tensor roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -137,6 +139,26 @@ def measured_peak_hbm():
         with open(p) as f:
             return float(json.load(f)["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_peak_tensor():
+    """Dense fp16/bf16 tensor peak in TFLOP/s: the measured cuBLAS bf16 burst figure (fp16
+    has the same nominal rate), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 same nominal rate)"
+    return 1900.0, "fallback"
+
+
+PREFILL_CHUNK = 2048   # prompt-chunk attention sample: the last chunk of the prompt
+
+
+def prefill_flops(n_q_heads, head_dim, pos0, n_q):
+    """Algorithmic FLOPs of causal chunk attention: 2 (QK) + 2 (PV) multiply-adds per
+    (query head, coordinate, visible key); query j sees pos0 + j + 1 keys."""
+    pairs = n_q * pos0 + n_q * (n_q + 1) // 2
+    return 4.0 * n_q_heads * head_dim * pairs
 
 
 # ------------------------------------------------------------------ multi-rank timing
@@ -294,6 +316,30 @@ def run_ours(args, rank, world, local_rank, dist):
     # (the encode graph rewrites the prefill rows with identical codes; rows >= T keep the
     #  decoded tokens)
 
+    # prompt-chunk attention (tensor-bound, timed alone): the last PREFILL_CHUNK queries of
+    # the prompt, positions T - PREFILL_CHUNK .. T - 1, over every layer's cache
+    pf_pos0 = T - PREFILL_CHUNK
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    q_pf = torch.randn((PREFILL_CHUNK, Hq, D), generator=gen, device=dev).half()
+    out_pf = torch.empty((PREFILL_CHUNK, Hq, D), dtype=torch.float32, device=dev)
+
+    def prefill_layers():
+        for l in range(L):
+            tq.attn_prefill(kc[l], vc[l], q_pf, out_pf, pos0=pf_pos0)
+
+    prefill_layers()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pf_reps = 2
+    e0.record()
+    for _ in range(pf_reps):
+        prefill_layers()
+    e1.record()
+    torch.cuda.synchronize()
+    pf_ms = e0.elapsed_time(e1) / pf_reps        # all layers
+    assert torch.isfinite(out_pf).all() and tq.device_status() == 0
+
     # end to end through the public API with host buffers: pinned host -> device copies of
     # every step's inputs and device -> host reads of every decode iteration's output
     out_host = torch.empty((S, L, Hq, D), dtype=torch.float32, pin_memory=True)
@@ -333,6 +379,8 @@ def run_ours(args, rank, world, local_rank, dist):
     e_bytes = encode_bytes_per_token(w, tt) // 2 * T
     e_gbs = e_bytes / (enc_launch_ms / 1e3) / 1e9
     h2d = kv_host.numel() * 2 + S * (new_host[0].numel() + q_host[0].numel()) * 2
+    tpeak, tpeak_kind = measured_peak_tensor()
+    pf_tflops = prefill_flops(Hq, D, pf_pos0, PREFILL_CHUNK) * L / (pf_ms / 1e3) / 1e12
     d2h = S * L * Hq * D * 4
     line = {
         "metric": "turbo3 decode-attn tokens/s & encode GB/s at 32K ctx; % of HBM peak",
@@ -368,6 +416,15 @@ def run_ours(args, rank, world, local_rank, dist):
         "e2e": {"value": world * n_e2e * S / (e2e_dec_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "encode_gbs": world * n_e2e * enc_bytes / (e2e_pre_ms / 1e3) / 1e9},
+        "prefill": {
+            "metric": f"prompt-chunk attention tokens/s ({PREFILL_CHUNK}-token chunk at position "
+                      f"{pf_pos0}, {L} layers)",
+            "value": PREFILL_CHUNK / (pf_ms / 1e3), "unit": "tokens/s", "ms": pf_ms,
+            "roofline": {"kernel": "tq_attn_prefill", "bound": "tensor",
+                         "achieved": pf_tflops, "peak": tpeak, "unit": "TFLOP/s",
+                         "frac": pf_tflops / tpeak, "peak_source": tpeak_kind, "traffic": None,
+                         "flops_per_launch": prefill_flops(Hq, D, pf_pos0, PREFILL_CHUNK),
+                         "launch_ms": pf_ms / L}},
         "gpu_launches": K * (L + S * L * 3),
         "clocks": clk,
         "device_status": status,
