@@ -70,6 +70,13 @@ def _load():
     lib.oracle_dense_attention.argtypes = [P, P, P, i64, i32, i32, i32, dbl, P]
     lib.oracle_attn_decode.argtypes = [i32, i32, P, P, P, i64, i32, i32, i32, dbl, P, P, P]
     lib.oracle_attn_prefill.argtypes = [i32, i32, P, P, P, i64, i64, i32, i32, i32, dbl, P, P, P]
+    lib.oracle_encode_block_v.argtypes = [i32, P, P, P, P, P]
+    lib.oracle_decode_block_v.argtypes = [i32, P, P, P, P]
+    lib.oracle_encode_rows_v.argtypes = [i32, P, i64, i32, i32, i64, P, P, P, P]
+    lib.oracle_decode_rows_v.argtypes = [i32, P, i64, i32, i32, P, P, P]
+    lib.oracle_attn_decode_v.argtypes = [i32, i32, P, P, P, i64, i32, i32, i32, dbl, P, P, P, P, P]
+    lib.oracle_attn_prefill_v.argtypes = [i32, i32, P, P, P, i64, i64, i32, i32, i32, dbl, P, P,
+                                          P, P, P]
     _lib = lib
     return lib
 
@@ -131,20 +138,43 @@ def type_codebook(tq_type: int):
     return c, t
 
 
-def encode_block(tq_type: int, x_f16_bits: np.ndarray) -> np.ndarray:
-    _, t = type_codebook(tq_type)
+class Variant(ctypes.Structure):
+    """oracle_variant: sign bits of the random-sign Hadamard W D (bit i of the 128-bit
+    mask, word i // 32, negates coordinate i) and the norm-correction flag."""
+    _fields_ = [("signs", ctypes.c_uint32 * 4), ("norm_correction", ctypes.c_int32)]
+
+
+def variant(signs=None, norm_correction=False):
+    """A Variant from a 128-entry 0/1 array (or an int mask) and a flag; None for none."""
+    if signs is None and not norm_correction:
+        return None
+    v = Variant()
+    if signs is not None:
+        mask = signs if isinstance(signs, int) else sum(int(b) << i for i, b in enumerate(signs))
+        for w in range(4):
+            v.signs[w] = (mask >> (32 * w)) & 0xFFFFFFFF
+    v.norm_correction = 1 if norm_correction else 0
+    return v
+
+
+def _vref(v):
+    return ctypes.byref(v) if v is not None else None
+
+
+def encode_block(tq_type: int, x_f16_bits: np.ndarray, var=None) -> np.ndarray:
+    c, t = type_codebook(tq_type)
     x = np.ascontiguousarray(x_f16_bits, dtype=np.uint16)
     assert x.size == BLOCK
     out = np.zeros(block_bytes(tq_type), np.uint8)
-    _load().oracle_encode_block(tq_type, _ptr(x), _ptr(t), _ptr(out))
+    _load().oracle_encode_block_v(tq_type, _ptr(x), _ptr(t), _ptr(c), _vref(var), _ptr(out))
     return out
 
 
-def decode_block(tq_type: int, blk: np.ndarray) -> np.ndarray:
+def decode_block(tq_type: int, blk: np.ndarray, var=None) -> np.ndarray:
     c, _ = type_codebook(tq_type)
     b = np.ascontiguousarray(blk, dtype=np.uint8)
     out = np.zeros(BLOCK, np.float64)
-    _load().oracle_decode_block(tq_type, _ptr(b), _ptr(c), _ptr(out))
+    _load().oracle_decode_block_v(tq_type, _ptr(b), _ptr(c), _vref(var), _ptr(out))
     return out
 
 
@@ -157,25 +187,27 @@ def unpack_block(tq_type: int, blk: np.ndarray):
 
 
 def encode_rows(tq_type: int, src_f16: np.ndarray, n_kv_heads: int, head_dim: int,
-                src_stride: int | None = None) -> np.ndarray:
+                src_stride: int | None = None, var=None) -> np.ndarray:
     """src_f16: uint16 (fp16 bits) or float16 array whose first axis is tokens."""
-    _, t = type_codebook(tq_type)
+    c, t = type_codebook(tq_type)
     src = np.ascontiguousarray(src_f16).view(np.uint16)
     n_tokens = src.shape[0]
     stride = n_kv_heads * head_dim if src_stride is None else src_stride
     nb = head_dim // BLOCK
     out = np.zeros((n_tokens, n_kv_heads * nb * block_bytes(tq_type)), np.uint8)
-    _load().oracle_encode_rows(tq_type, _ptr(src), n_tokens, n_kv_heads, head_dim, stride,
-                               _ptr(t), _ptr(out))
+    _load().oracle_encode_rows_v(tq_type, _ptr(src), n_tokens, n_kv_heads, head_dim, stride,
+                                 _ptr(t), _ptr(c), _vref(var), _ptr(out))
     return out
 
 
-def decode_rows(tq_type: int, rows: np.ndarray, n_kv_heads: int, head_dim: int) -> np.ndarray:
+def decode_rows(tq_type: int, rows: np.ndarray, n_kv_heads: int, head_dim: int,
+                var=None) -> np.ndarray:
     c, _ = type_codebook(tq_type)
     r = np.ascontiguousarray(rows, dtype=np.uint8)
     n_tokens = r.shape[0]
     out = np.zeros((n_tokens, n_kv_heads, head_dim), np.float64)
-    _load().oracle_decode_rows(tq_type, _ptr(r), n_tokens, n_kv_heads, head_dim, _ptr(c), _ptr(out))
+    _load().oracle_decode_rows_v(tq_type, _ptr(r), n_tokens, n_kv_heads, head_dim, _ptr(c),
+                                 _vref(var), _ptr(out))
     return out
 
 
@@ -194,7 +226,7 @@ def dense_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_kv_heads: int
 
 def attn_decode(type_k: int, type_v: int, k_rows: np.ndarray, v_rows: np.ndarray,
                 q_f16: np.ndarray, n_tokens: int, n_q_heads: int, n_kv_heads: int,
-                head_dim: int, scale: float) -> np.ndarray:
+                head_dim: int, scale: float, var_k=None, var_v=None) -> np.ndarray:
     """Attention of one query row over the first n_tokens packed rows -> [Hq][D] f64."""
     ck, _ = type_codebook(type_k)
     cv, _ = type_codebook(type_v)
@@ -202,14 +234,15 @@ def attn_decode(type_k: int, type_v: int, k_rows: np.ndarray, v_rows: np.ndarray
     vr = np.ascontiguousarray(v_rows, dtype=np.uint8)
     q = np.ascontiguousarray(q_f16).view(np.uint16)
     out = np.zeros((n_q_heads, head_dim), np.float64)
-    _load().oracle_attn_decode(type_k, type_v, _ptr(kr), _ptr(vr), _ptr(q), n_tokens, n_q_heads,
-                               n_kv_heads, head_dim, float(scale), _ptr(ck), _ptr(cv), _ptr(out))
+    _load().oracle_attn_decode_v(type_k, type_v, _ptr(kr), _ptr(vr), _ptr(q), n_tokens, n_q_heads,
+                                 n_kv_heads, head_dim, float(scale), _ptr(ck), _ptr(cv),
+                                 _vref(var_k), _vref(var_v), _ptr(out))
     return out
 
 
 def attn_prefill(type_k: int, type_v: int, k_rows: np.ndarray, v_rows: np.ndarray,
                  q_f16: np.ndarray, pos0: int, n_kv_heads: int, head_dim: int,
-                 scale: float) -> np.ndarray:
+                 scale: float, var_k=None, var_v=None) -> np.ndarray:
     """Causal attention of a prompt chunk: q_f16 [n_q][Hq][D], query j at position pos0 + j
     over packed rows 0 .. pos0 + j  ->  [n_q][Hq][D] f64."""
     ck, _ = type_codebook(type_k)
@@ -220,7 +253,8 @@ def attn_prefill(type_k: int, type_v: int, k_rows: np.ndarray, v_rows: np.ndarra
     vr = np.ascontiguousarray(v_rows, dtype=np.uint8)
     assert kr.shape[0] >= pos0 + n_q and vr.shape[0] >= pos0 + n_q
     out = np.zeros((n_q, n_q_heads, head_dim), np.float64)
-    _load().oracle_attn_prefill(type_k, type_v, _ptr(kr), _ptr(vr), _ptr(q), pos0, n_q, n_q_heads,
-                                n_kv_heads, head_dim, float(scale), _ptr(ck), _ptr(cv), _ptr(out))
+    _load().oracle_attn_prefill_v(type_k, type_v, _ptr(kr), _ptr(vr), _ptr(q), pos0, n_q,
+                                  n_q_heads, n_kv_heads, head_dim, float(scale), _ptr(ck),
+                                  _ptr(cv), _vref(var_k), _vref(var_v), _ptr(out))
     return out
 

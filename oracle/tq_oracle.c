@@ -269,13 +269,23 @@ void oracle_unpack_block(int type, const uint8_t *blk, uint8_t *codes, uint16_t 
 
 /* ---------------------------------------------------------------- encode / decode */
 
-void oracle_encode_block(int type, const uint16_t *x_f16, const float *thresholds,
-                         uint8_t *out)
+static int sign_bit(const oracle_variant *var, int i)
+{
+    return var ? (int)((var->signs[i / 32] >> (i % 32)) & 1u) : 0;
+}
+
+void oracle_encode_block_v(int type, const uint16_t *x_f16, const float *thresholds,
+                           const float *centroids, const oracle_variant *var, uint8_t *out)
 {
     const int levels = 1 << type;
     float x[ORACLE_BLOCK], s[ORACLE_BLOCK], z[ORACLE_BLOCK];
     uint8_t codes[ORACLE_BLOCK];
     for (int i = 0; i < ORACLE_BLOCK; ++i) x[i] = oracle_f16_to_f32(x_f16[i]);
+
+    /* 0. variant: the rotation is W D, so coordinates with a sign bit are negated first
+     *    (exact; the norm does not change) */
+    for (int i = 0; i < ORACLE_BLOCK; ++i)
+        if (sign_bit(var, i)) x[i] = -x[i];
 
     /* 1. norm: pairwise tree, level by level, element i pairs with i + len/2 */
     for (int i = 0; i < ORACLE_BLOCK; ++i) s[i] = x[i] * x[i];
@@ -283,7 +293,8 @@ void oracle_encode_block(int type, const uint16_t *x_f16, const float *threshold
         for (int i = 0; i < len / 2; ++i) s[i] = s[i] + s[i + len / 2];
     float n = sqrtf(s[0]);
 
-    /* 2. stored norm, saturated to the largest finite binary16 */
+    /* 2. stored norm, saturated to the largest finite binary16 (set in step 5 for the
+     *    norm-correcting variant) */
     uint16_t norm16 = oracle_f32_to_f16(n < 65504.0f ? n : 65504.0f);
 
     /* 3. rotation: unnormalised Walsh-Hadamard butterflies */
@@ -305,11 +316,30 @@ void oracle_encode_block(int type, const uint16_t *x_f16, const float *threshold
         codes[i] = (uint8_t)(signbit(y) ? levels / 2 - 1 - m : levels / 2 + m);
     }
 
+    /* 5b. variant: store |x| / |c|, |c| the norm of the centroid vector of the codes
+     *     (same pairwise tree as step 1, then an IEEE sqrt and divide), so that the decoded
+     *     block keeps the norm of its input up to the fp16 rounding */
+    if (var && var->norm_correction) {
+        float c2[ORACLE_BLOCK];
+        for (int i = 0; i < ORACLE_BLOCK; ++i) c2[i] = centroids[codes[i]] * centroids[codes[i]];
+        for (int len = ORACLE_BLOCK; len > 1; len /= 2)
+            for (int i = 0; i < len / 2; ++i) c2[i] = c2[i] + c2[i + len / 2];
+        float r = n / sqrtf(c2[0]);
+        norm16 = oracle_f32_to_f16(r < 65504.0f ? r : 65504.0f);
+    }
+
     /* 6. pack */
     pack_block(type, norm16, codes, out);
 }
 
-void oracle_decode_block(int type, const uint8_t *blk, const float *centroids, double *out)
+void oracle_encode_block(int type, const uint16_t *x_f16, const float *thresholds,
+                         uint8_t *out)
+{
+    oracle_encode_block_v(type, x_f16, thresholds, NULL, NULL, out);
+}
+
+void oracle_decode_block_v(int type, const uint8_t *blk, const float *centroids,
+                           const oracle_variant *var, double *out)
 {
     uint8_t codes[ORACLE_BLOCK];
     uint16_t norm16;
@@ -317,12 +347,26 @@ void oracle_decode_block(int type, const uint8_t *blk, const float *centroids, d
     for (int i = 0; i < ORACLE_BLOCK; ++i) out[i] = (double)centroids[codes[i]];
     oracle_fwht_f64(out, ORACLE_BLOCK);     /* W is its own inverse up to 1/128 */
     double sc = (double)oracle_f16_to_f32(norm16) / sqrt(128.0);
-    for (int i = 0; i < ORACLE_BLOCK; ++i) out[i] *= sc;
+    for (int i = 0; i < ORACLE_BLOCK; ++i) out[i] *= sign_bit(var, i) ? -sc : sc;   /* D W c */
+}
+
+void oracle_decode_block(int type, const uint8_t *blk, const float *centroids, double *out)
+{
+    oracle_decode_block_v(type, blk, centroids, NULL, out);
 }
 
 void oracle_encode_rows(int type, const uint16_t *src, int64_t n_tokens,
                         int n_kv_heads, int head_dim, int64_t src_stride,
                         const float *thresholds, uint8_t *dst)
+{
+    oracle_encode_rows_v(type, src, n_tokens, n_kv_heads, head_dim, src_stride, thresholds,
+                         NULL, NULL, dst);
+}
+
+void oracle_encode_rows_v(int type, const uint16_t *src, int64_t n_tokens,
+                          int n_kv_heads, int head_dim, int64_t src_stride,
+                          const float *thresholds, const float *centroids,
+                          const oracle_variant *var, uint8_t *dst)
 {
     const size_t bb = oracle_block_bytes(type);
     const int nb = head_dim / ORACLE_BLOCK;
@@ -331,13 +375,20 @@ void oracle_encode_rows(int type, const uint16_t *src, int64_t n_tokens,
             for (int b = 0; b < nb; ++b) {
                 const uint16_t *x = src + t * src_stride + (int64_t)h * head_dim + b * ORACLE_BLOCK;
                 uint8_t *o = dst + ((size_t)t * (size_t)(n_kv_heads * nb) + (size_t)(h * nb + b)) * bb;
-                oracle_encode_block(type, x, thresholds, o);
+                oracle_encode_block_v(type, x, thresholds, centroids, var, o);
             }
 }
 
 void oracle_decode_rows(int type, const uint8_t *src, int64_t n_tokens,
                         int n_kv_heads, int head_dim, const float *centroids,
                         double *dst)
+{
+    oracle_decode_rows_v(type, src, n_tokens, n_kv_heads, head_dim, centroids, NULL, dst);
+}
+
+void oracle_decode_rows_v(int type, const uint8_t *src, int64_t n_tokens,
+                          int n_kv_heads, int head_dim, const float *centroids,
+                          const oracle_variant *var, double *dst)
 {
     const size_t bb = oracle_block_bytes(type);
     const int nb = head_dim / ORACLE_BLOCK;
@@ -346,7 +397,7 @@ void oracle_decode_rows(int type, const uint8_t *src, int64_t n_tokens,
             for (int b = 0; b < nb; ++b) {
                 const uint8_t *blk = src + ((size_t)t * (size_t)(n_kv_heads * nb) + (size_t)(h * nb + b)) * bb;
                 double *o = dst + (t * n_kv_heads + h) * (int64_t)head_dim + b * ORACLE_BLOCK;
-                oracle_decode_block(type, blk, centroids, o);
+                oracle_decode_block_v(type, blk, centroids, var, o);
             }
 }
 
@@ -391,6 +442,17 @@ void oracle_attn_decode(int type_k, int type_v, const uint8_t *k_rows,
                         int head_dim, double scale, const float *centroids_k,
                         const float *centroids_v, double *out)
 {
+    oracle_attn_decode_v(type_k, type_v, k_rows, v_rows, q_f16, n_tokens, n_q_heads,
+                         n_kv_heads, head_dim, scale, centroids_k, centroids_v, NULL, NULL, out);
+}
+
+void oracle_attn_decode_v(int type_k, int type_v, const uint8_t *k_rows,
+                          const uint8_t *v_rows, const uint16_t *q_f16,
+                          int64_t n_tokens, int n_q_heads, int n_kv_heads,
+                          int head_dim, double scale, const float *centroids_k,
+                          const float *centroids_v, const oracle_variant *var_k,
+                          const oracle_variant *var_v, double *out)
+{
     size_t per_tok = (size_t)n_kv_heads * (size_t)head_dim;
     size_t n_el = (size_t)(n_tokens > 0 ? n_tokens : 0) * per_tok;
     double *k = (double *)malloc((n_el ? n_el : 1) * sizeof(double));
@@ -399,8 +461,8 @@ void oracle_attn_decode(int type_k, int type_v, const uint8_t *k_rows,
     if (!k || !v || !q) { free(k); free(v); free(q); return; }
     for (int64_t i = 0; i < (int64_t)n_q_heads * head_dim; ++i) q[i] = oracle_f16_to_f32(q_f16[i]);
     if (n_tokens > 0) {
-        oracle_decode_rows(type_k, k_rows, n_tokens, n_kv_heads, head_dim, centroids_k, k);
-        oracle_decode_rows(type_v, v_rows, n_tokens, n_kv_heads, head_dim, centroids_v, v);
+        oracle_decode_rows_v(type_k, k_rows, n_tokens, n_kv_heads, head_dim, centroids_k, var_k, k);
+        oracle_decode_rows_v(type_v, v_rows, n_tokens, n_kv_heads, head_dim, centroids_v, var_v, v);
     }
     oracle_dense_attention(q, k, v, n_tokens, n_q_heads, n_kv_heads, head_dim, scale, out);
     free(k); free(v); free(q);
@@ -412,6 +474,17 @@ void oracle_attn_prefill(int type_k, int type_v, const uint8_t *k_rows,
                          double scale, const float *centroids_k, const float *centroids_v,
                          double *out)
 {
+    oracle_attn_prefill_v(type_k, type_v, k_rows, v_rows, q_f16, pos0, n_q, n_q_heads,
+                          n_kv_heads, head_dim, scale, centroids_k, centroids_v, NULL, NULL, out);
+}
+
+void oracle_attn_prefill_v(int type_k, int type_v, const uint8_t *k_rows,
+                           const uint8_t *v_rows, const uint16_t *q_f16, int64_t pos0,
+                           int64_t n_q, int n_q_heads, int n_kv_heads, int head_dim,
+                           double scale, const float *centroids_k, const float *centroids_v,
+                           const oracle_variant *var_k, const oracle_variant *var_v,
+                           double *out)
+{
     const int64_t n_rows = pos0 + n_q;
     const size_t per_tok = (size_t)n_kv_heads * (size_t)head_dim;
     const size_t per_q = (size_t)n_q_heads * (size_t)head_dim;
@@ -421,8 +494,8 @@ void oracle_attn_prefill(int type_k, int type_v, const uint8_t *k_rows,
     double *q = (double *)malloc((per_q ? per_q : 1) * sizeof(double));
     if (!k || !v || !q) { free(k); free(v); free(q); return; }
     if (n_rows > 0) {
-        oracle_decode_rows(type_k, k_rows, n_rows, n_kv_heads, head_dim, centroids_k, k);
-        oracle_decode_rows(type_v, v_rows, n_rows, n_kv_heads, head_dim, centroids_v, v);
+        oracle_decode_rows_v(type_k, k_rows, n_rows, n_kv_heads, head_dim, centroids_k, var_k, k);
+        oracle_decode_rows_v(type_v, v_rows, n_rows, n_kv_heads, head_dim, centroids_v, var_v, v);
     }
     /* query j sees the first pos0 + j + 1 rows */
     for (int64_t j = 0; j < n_q; ++j) {

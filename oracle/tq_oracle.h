@@ -156,6 +156,50 @@ void oracle_attn_prefill(int type_k, int type_v, const uint8_t *k_rows,
                          double scale, const float *centroids_k, const float *centroids_v,
                          double *out);
 
+/* ---------------------------------------------------------------- variants
+ * Quality variants of the method.  NULL selects the plain method everywhere.
+ *  - signs: bit i (word i / 32, bit i % 32) negates coordinate i of every block before the
+ *    rotation, which becomes W D: a random-sign Hadamard.  [TQ] "What TurboQuant does
+ *    differently": a random orthogonal rotation spreads the energy, and the FWHT is said to
+ *    have the same spreading in expectation; W D is the randomised form of that FWHT.  The
+ *    inverse is D W, so decode negates the same coordinates after the inverse rotation.
+ *    The sign bits are an input (the caller draws them).
+ *  - norm_correction: store |x| / |c|, where |c| is the norm of the block's centroid vector
+ *    (pairwise fp32 tree of c_i^2 as for the norm, IEEE sqrt and divide), so that a decoded
+ *    block keeps the norm of its input up to the fp16 rounding.  Not on the pages. */
+typedef struct oracle_variant {
+    uint32_t signs[4];
+    int32_t norm_correction;
+} oracle_variant;
+
+/* oracle_encode_block with a variant; centroids (2^type fp32) are read only for the norm
+ * correction. */
+void oracle_encode_block_v(int type, const uint16_t *x_f16, const float *thresholds,
+                           const float *centroids, const oracle_variant *var, uint8_t *out);
+/* oracle_decode_block with a variant: x_hat = D * (norm / sqrt(128)) * W * c. */
+void oracle_decode_block_v(int type, const uint8_t *blk, const float *centroids,
+                           const oracle_variant *var, double *out);
+void oracle_encode_rows_v(int type, const uint16_t *src, int64_t n_tokens,
+                          int n_kv_heads, int head_dim, int64_t src_stride,
+                          const float *thresholds, const float *centroids,
+                          const oracle_variant *var, uint8_t *dst);
+void oracle_decode_rows_v(int type, const uint8_t *src, int64_t n_tokens,
+                          int n_kv_heads, int head_dim, const float *centroids,
+                          const oracle_variant *var, double *dst);
+/* Attention over caches encoded with variants var_k / var_v (dequantised with them). */
+void oracle_attn_decode_v(int type_k, int type_v, const uint8_t *k_rows,
+                          const uint8_t *v_rows, const uint16_t *q_f16,
+                          int64_t n_tokens, int n_q_heads, int n_kv_heads,
+                          int head_dim, double scale, const float *centroids_k,
+                          const float *centroids_v, const oracle_variant *var_k,
+                          const oracle_variant *var_v, double *out);
+void oracle_attn_prefill_v(int type_k, int type_v, const uint8_t *k_rows,
+                           const uint8_t *v_rows, const uint16_t *q_f16, int64_t pos0,
+                           int64_t n_q, int n_q_heads, int n_kv_heads, int head_dim,
+                           double scale, const float *centroids_k, const float *centroids_v,
+                           const oracle_variant *var_k, const oracle_variant *var_v,
+                           double *out);
+
 #ifdef __cplusplus
 }
 #endif
