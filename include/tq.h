@@ -89,6 +89,20 @@ typedef struct tq_cache {
     int32_t max_pages_per_seq;  /* paged: columns of page_table */
     const int32_t *page_table;  /* paged: device int32 [n_seqs][max_pages_per_seq] */
     int64_t n_pages;            /* paged: pages in the pool at base */
+    /* Quality variants (all zero: the plain method).
+     * rotation_signs: bit i (word i / 32, bit i % 32) negates coordinate i of every
+     *   128-value block before the rotation, which becomes W D, a random-sign Hadamard
+     *   ("What TurboQuant does differently": a random orthogonal rotation, whose energy
+     *   spreading the FWHT matches in expectation).  Decode negates the same coordinates
+     *   after the inverse rotation (D W); attention rotates queries with the K cache's
+     *   signs and un-rotates outputs with the V cache's.  The caller draws the bits; they
+     *   must stay the same for the life of the cache.
+     * norm_correction: 0 stores |x|; 1 stores |x| / |c|, where |c| is the norm of the
+     *   block's centroid vector (pairwise fp32 sum of c_i^2, IEEE sqrt and divide), so a
+     *   decoded block keeps the norm of its input up to the fp16 rounding.  It changes only
+     *   the stored norm; decode and attention are unchanged.  Not on the pages. */
+    uint32_t rotation_signs[4];
+    int32_t norm_correction;
 } tq_cache;
 
 /* 50 (turbo3) or 34 (turbo2); 0 for an unknown type.  "How small does it get":

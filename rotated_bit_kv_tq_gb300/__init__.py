@@ -53,11 +53,14 @@ class KVCache:
 
     Contiguous: ``capacity_tokens`` rows per sequence.  Paged: pass ``page_tokens`` and an
     int32 device ``page_table`` [n_seqs, max_pages]; the pool holds ``n_pages`` pages.
+    Variants: ``rotation_signs`` (a 128-bit int or 128 0/1 values: coordinate i negated
+    before the rotation, W D) and ``norm_correction`` (store |x| / |c|).
     """
 
     def __init__(self, tq_type: int, n_kv_heads: int, head_dim: int, *, n_seqs: int = 1,
                  capacity_tokens: int = 0, page_tokens: int = 0, page_table=None,
-                 n_pages: int = 0, device=None, buffer=None):
+                 n_pages: int = 0, device=None, buffer=None, rotation_signs=None,
+                 norm_correction: bool = False):
         import torch
         self.type, self.n_kv_heads, self.head_dim = tq_type, n_kv_heads, head_dim
         self.row_bytes = row_bytes(tq_type, n_kv_heads, head_dim)
@@ -72,6 +75,12 @@ class KVCache:
         self.view = TqCache(tq_type, n_kv_heads, head_dim, page_tokens, buffer.data_ptr(),
                             capacity_tokens, n_seqs, page_table.shape[1] if page_table is not None else 0,
                             page_table.data_ptr() if page_table is not None else None, n_pages)
+        if rotation_signs is not None:
+            mask = (rotation_signs if isinstance(rotation_signs, int)
+                    else sum(int(b) << i for i, b in enumerate(rotation_signs)))
+            for w in range(4):
+                self.view.rotation_signs[w] = (mask >> (32 * w)) & 0xFFFFFFFF
+        self.view.norm_correction = 1 if norm_correction else 0
 
     @property
     def nbytes(self) -> int:

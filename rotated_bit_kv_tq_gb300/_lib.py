@@ -41,6 +41,8 @@ class TqCache(ctypes.Structure):
         ("max_pages_per_seq", ctypes.c_int32),
         ("page_table", ctypes.c_void_p),
         ("n_pages", ctypes.c_int64),
+        ("rotation_signs", ctypes.c_uint32 * 4),
+        ("norm_correction", ctypes.c_int32),
     ]
 
 

@@ -68,6 +68,10 @@ CacheView make_view(const tq_cache &c) {
     v.max_pages = c.max_pages_per_seq;
     v.n_seqs = c.n_seqs;
     v.row_bytes = (int32_t)tq_row_bytes(c.type, c.n_kv_heads, c.head_dim);
+    for (int w = 0; w < 4; ++w) v.signs[w] = c.rotation_signs[w];
+    v.norm_correction = c.norm_correction;
+    v.has_signs = (c.rotation_signs[0] | c.rotation_signs[1] | c.rotation_signs[2] |
+                   c.rotation_signs[3]) != 0;
     return v;
 }
 
@@ -79,6 +83,7 @@ tq_status validate_cache(const tq_cache *c) {
     if (reinterpret_cast<uintptr_t>(c->base) % 16 != 0) return TQ_ERR_INVALID_ARGUMENT;
     if ((int64_t)c->n_kv_heads * (c->head_dim / kBlock) > 128) return TQ_ERR_UNSUPPORTED;
     if (c->page_tokens < 0) return TQ_ERR_INVALID_ARGUMENT;
+    if (c->norm_correction != 0 && c->norm_correction != 1) return TQ_ERR_INVALID_ARGUMENT;
     if (c->page_tokens == 0) {
         if (c->capacity_tokens < 1) return TQ_ERR_INVALID_ARGUMENT;
     } else {

@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
         float v[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = __half2float(qp[e]);
+        apply_signs4(v, p.kc, 4 * lane);   // rotation W D of the K cache
         warp_fwht4(v, lane);
 #pragma unroll
         for (int e = 0; e < 4; ++e) qs[h * D + b * kBlock + 4 * lane + e] = v[e] * qscale;
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     const float inv = L > 0.f ? kInvSqrt128 / L : 0.f;
     // inverse rotation (1/sqrt(128)) W o_b, values 4*lane .. 4*lane+3
     warp_fwht4(v, lane);
+    apply_signs4(v, p.vc, 4 * lane);     // inverse D W of the V cache
     float4 o4 = make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
     *reinterpret_cast<float4 *>(p.out + ((int64_t)seq * p.n_q_heads + h) * D + b * kBlock + 4 * lane) = o4;
 }

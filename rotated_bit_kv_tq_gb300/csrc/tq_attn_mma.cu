@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
         const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
         const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
         float v[4] = {f01.x, f01.y, f23.x, f23.y};
+        apply_signs4(v, p.kc, 4 * lane);   // rotation W D of the K cache
         warp_fwht4(v, lane);
         uint2 o;
         o.x = pack_half2(v[0] * p.score_scale, v[1] * p.score_scale);

@@ -72,7 +72,11 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
     }
     const uint16_t nb = (uint16_t)(b[0] | (b[1] << 8));
     const float sc = __half2float(__ushort_as_half(nb)) * kInvSqrt128;
-    *out = make_float4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+    // rotation-sign variant: D W c, coordinate i negated when its sign bit is set
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = __uint_as_float(__float_as_uint(v[e] * sc) ^ sign_mask(p.src, i0 + e));
+    *out = make_float4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace

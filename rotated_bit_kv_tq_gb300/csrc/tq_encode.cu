@@ -74,8 +74,21 @@ __device__ __forceinline__ uint32_t collect2(uint32_t w, float v) {
     return __funnelshift_l(__float_as_uint(v), w, 2);
 }
 
+// Squared centroid of a value's code: it depends only on the magnitude index
+// m = #{positive thresholds below |y|} (the codebook is symmetric).
 template <int TYPE>
-__device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t *out) {
+__device__ __forceinline__ float code_sq(const Codebook &cb, float y) {
+    constexpr int L = 1 << TYPE;
+    const float a = fabsf(y);
+    int m = a > cb.threshold[L / 2] ? 1 : 0;
+    if (TYPE == TQ_TURBO3) m += (a > cb.threshold[5] ? 1 : 0) + (a > cb.threshold[6] ? 1 : 0);
+    const float c = cb.centroid[L / 2 + m];
+    return __fmul_rn(c, c);
+}
+
+template <int TYPE>
+__device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t *out,
+                                           const CacheView &cv) {
     const Codebook &cb = c_codebook[cb_index(TYPE)];
     // ---- 1. load and convert once
     float x[kBlock];
@@ -89,6 +102,11 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
             x[8 * j + 2 * e] = t.x;
             x[8 * j + 2 * e + 1] = t.y;
         }
+    }
+    // rotation-sign variant: the rotation is W D, so flagged coordinates are negated first
+    if (cv.has_signs) {
+#pragma unroll
+        for (int i = 0; i < kBlock; ++i) x[i] = __uint_as_float(__float_as_uint(x[i]) ^ sign_mask(cv, i));
     }
     // ---- 2. norm: pairwise tree, element i pairs with i + len/2 at every level
     float s1[64];
@@ -189,9 +207,23 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
             V[u] = ~sv;
         }
     }
+    // norm-correction variant: store |x| / |c|, |c| over the same pairwise tree as the norm
+    uint16_t norm_out = norm16;
+    if (cv.norm_correction) {
+        float c2[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            c2[i] = __fadd_rn(code_sq<TYPE>(cb, x[i]), code_sq<TYPE>(cb, x[i + 64]));
+#pragma unroll
+        for (int len = 64; len > 1; len >>= 1)
+#pragma unroll
+            for (int i = 0; i < len / 2; ++i) c2[i] = __fadd_rn(c2[i], c2[i + len / 2]);
+        const float r = __fdiv_rn(n, __fsqrt_rn(c2[0]));
+        norm_out = __half_as_ushort(__float2half_rn(fminf(r, 65504.0f)));
+    }
     // ---- 6. stage the packed block (2-byte aligned in shared memory)
     uint16_t *o = reinterpret_cast<uint16_t *>(out);
-    o[0] = norm16;
+    o[0] = norm_out;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
         o[1 + 2 * w] = (uint16_t)(W[w] & 0xffffu);
@@ -238,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 3) encode_kernel(const EncodeParams 
 
         const int nblk = rows * p.bpr;
         const int f = threadIdx.x;
-        if (f < nblk) encode_one<TYPE>(sm.in[it & 1] + f * 256, f, sm.out + f * B);
+        if (f < nblk) encode_one<TYPE>(sm.in[it & 1] + f * 256, f, sm.out + f * B, p.dst);
         __syncthreads();
 
         // ---- write whole rows out
@@ -317,6 +349,10 @@ __global__ void __launch_bounds__(32 * kWarpPathWarps) encode_warp_kernel(const 
     const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
     const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
     float x[4] = {f01.x, f01.y, f23.x, f23.y};
+    if (p.dst.has_signs) {   // rotation-sign variant: W D
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = __uint_as_float(__float_as_uint(x[e]) ^ sign_mask(p.dst, 4 * lane + e));
+    }
     // norm
     float sq[4];
 #pragma unroll
@@ -326,7 +362,7 @@ __global__ void __launch_bounds__(32 * kWarpPathWarps) encode_warp_kernel(const 
 #pragma unroll
         for (int e = 0; e < 4; ++e) sq[e] = __fadd_rn(sq[e], __shfl_xor_sync(0xffffffffu, sq[e], off));
     const float n = __fsqrt_rn(__fadd_rn(__fadd_rn(sq[0], sq[2]), __fadd_rn(sq[1], sq[3])));
-    const uint16_t norm16 = __half_as_ushort(__float2half_rn(fminf(n, 65504.0f)));
+    uint16_t norm16 = __half_as_ushort(__float2half_rn(fminf(n, 65504.0f)));
     const float k = n > 0.0f ? __fdiv_rn(kInvSqrt128, n) : 0.0f;
     // butterflies
     {
@@ -348,10 +384,24 @@ __global__ void __launch_bounds__(32 * kWarpPathWarps) encode_warp_kernel(const 
     }
     // sign-magnitude quantiser: m = #{positive thresholds strictly below |y|},
     // code = signbit(y) ? L/2 - 1 - m : L/2 + m; pack into this lane's share of the words
+    float ys[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ys[e] = __fmul_rn(x[e], k);
+    if (p.dst.norm_correction) {   // store |x| / |c|, |c| over the norm's pairwise tree
+        float c2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c2[e] = code_sq<TYPE>(cb, ys[e]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c2[e] = __fadd_rn(c2[e], __shfl_xor_sync(0xffffffffu, c2[e], off));
+        const float cn = __fsqrt_rn(__fadd_rn(__fadd_rn(c2[0], c2[2]), __fadd_rn(c2[1], c2[3])));
+        norm16 = __half_as_ushort(__float2half_rn(fminf(__fdiv_rn(n, cn), 65504.0f)));
+    }
     uint32_t wlo = 0, whi = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float y = __fmul_rn(x[e], k);
+        const float y = ys[e];
         const float a = fabsf(y);
         uint32_t m = 0;
 #pragma unroll

@@ -39,7 +39,30 @@ struct CacheView {
     int32_t max_pages;
     int32_t n_seqs;
     int32_t row_bytes;
+    uint32_t signs[4];          // rotation_signs of tq_cache (all zero: plain FWHT)
+    int32_t norm_correction;
+    int32_t has_signs;          // any sign bit set
 };
+
+#if defined(__CUDACC__)
+// -1.0f-sign mask of coordinate i under a cache's rotation signs: 0x80000000 or 0.
+// (The word is picked with selects: a run-time index into a parameter array would copy
+// the array to local memory.)
+__device__ __forceinline__ uint32_t sign_mask(const CacheView &c, int i) {
+    const int w = i >> 5;
+    const uint32_t word = w == 0 ? c.signs[0] : w == 1 ? c.signs[1] : w == 2 ? c.signs[2] : c.signs[3];
+    return ((word >> (i & 31)) & 1u) << 31;
+}
+
+// Negate the values of coordinates i0 .. i0+3 whose rotation-sign bit is set (D v): on a
+// query before its rotation with the K cache's signs, on an output after its inverse
+// rotation with the V cache's.
+__device__ __forceinline__ void apply_signs4(float (&v)[4], const CacheView &c, int i0) {
+    if (!c.has_signs) return;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sign_mask(c, i0 + e));
+}
+#endif
 
 #if defined(__CUDACC__)
 // First device-side error of the current device (0 = none); read by tq_device_status.

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
             v[1] = f01.y;
             v[2] = f23.x;
             v[3] = f23.y;
+            apply_signs4(v, p.kc, 4 * lane);   // rotation W D of the K cache
             warp_fwht4(v, lane);
         }
         *reinterpret_cast<uint2 *>(qt + r * kKs + 4 * lane) =
@@ -309,6 +310,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const PrefillPar
         float4 a = *reinterpret_cast<const float4 *>(os + rr * kOs + 4 * lane);
         float v[4] = {a.x, a.y, a.z, a.w};
         warp_fwht4(v, lane);   // (1/sqrt(128)) W o, the 1/sqrt(128) folded into inv
+        apply_signs4(v, p.vc, 4 * lane);     // inverse D W of the V cache
         *reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)kBlock + 4 * lane) =
             make_float4(v[0], v[1], v[2], v[3]);
     }
