@@ -176,6 +176,9 @@ bool prefill_supported(const tq_cache &k, const tq_cache &v, int n_q_heads);
 tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, int32_t seq_id,
                          int64_t pos0, int64_t n_q, int n_q_heads, float scale, float *out,
                          cudaStream_t stream);
+tq_status launch_prefill_tc(const tq_cache &k, const tq_cache &v, const void *q, int32_t seq_id,
+                            int64_t pos0, int64_t n_q, int n_q_heads, float scale, float *out,
+                            cudaStream_t stream);
 
 // Host Lloyd-Max solver (tq_codebook.cpp).
 void solve_codebook(int levels, double *centroids);

@@ -36,6 +36,8 @@ constexpr int kKs = 136;                    // halfs per decoded row (128 + 8: l
 constexpr int kSlot = 64;                   // staged bytes per key: the block's covering 16-byte chunks
 constexpr int kOs = 132;                    // floats per output staging row
 constexpr float kPfLog2e = 1.4426950408889634f;
+// The 5th-generation tensor-core kernel (tq_prefill_tc.cu) takes every shape this one does.
+constexpr bool kUseTcgen05 = true;
 
 struct PrefillParams {
     CacheView kc, vc;
@@ -338,6 +340,8 @@ tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, in
                          cudaStream_t stream) {
     if (!prefill_supported(k, v, n_q_heads)) return TQ_ERR_UNSUPPORTED;
     if (n_q == 0) return TQ_OK;
+    if (kUseTcgen05)
+        return launch_prefill_tc(k, v, q, seq_id, pos0, n_q, n_q_heads, scale, out, stream);
     PrefillParams p;
     p.kc = make_view(k);
     p.vc = make_view(v);

@@ -1,0 +1,521 @@
+// tq_prefill_tc.cu -- causal prompt-chunk attention over the packed cache on the 5th-generation
+// tensor cores (tcgen05: operands in shared memory, accumulators in tensor memory).
+//
+// Same mathematics as tq_prefill.cu ("llama.cpp に TurboQuant を実装": prompt processing over the
+// compressed cache, dequantisation inside the attention tiles; TinyLLaMA article, section 7:
+// the query at position N attends to rows 0..N).  The work split follows the roles the
+// tensor-memory model suggests:
+//  - warps 0-3 (one thread per row of the 128-row tile, row = TMEM lane): rotate the queries
+//    into shared memory; per key tile read the scores S from TMEM, scale by |k|, mask, run
+//    the online softmax entirely inside the thread, write P (times |v|, fp16) to shared
+//    memory, rescale O in TMEM when the running maximum moved; at the end read O, divide,
+//    inverse-FWHT the row in registers and store it;
+//  - warps 4-7: stage each tile's block bytes (cp.async), decode them once into fp16
+//    centroid values laid out as the MMA operands (K: keys x coords, K-major; V: keys x
+//    coords with coords contiguous, MN-major), double-buffered;
+//  - warp 8: allocates TMEM and issues the MMAs from one thread: S[b] = Q~ K^T (M = 128
+//    rows, N = 128 keys, K = 128 coords) into one of two TMEM score buffers, so the scores
+//    of the next tile are computed while the softmax works on this one, and
+//    O += P V (N = 128 coords, K = 128 keys); completions arrive on mbarriers through
+//    tcgen05.commit.
+// Shared-memory operands use the no-swizzle canonical layout: 8 x 16-byte core matrices,
+// core matrices adjacent along K 128 bytes apart (LBO), 8-row groups along M/N 2048 bytes
+// apart (SBO).  Every wait is bounded; a timeout records TQ_ERR_DEVICE_TIMEOUT and the CTA
+// still releases its tensor memory.
+#include <cmath>
+
+#include "tq_internal.cuh"
+#include "tq_simd.cuh"
+#include "tq_codes.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kTcRows = 128;          // (query token, head) rows per CTA = TMEM lanes
+constexpr int kTcKeys = 128;          // keys per tile
+constexpr int kTcSoftmax = 128;       // threads of warps 0-3
+constexpr int kTcProducer = 128;      // threads of warps 4-7
+constexpr int kTcThreads = kTcSoftmax + kTcProducer + 32;
+constexpr int kTcSlot = 64;           // staged bytes per key and cache
+constexpr uint32_t kTcWaitLimit = 1u << 20;
+constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256,384)
+constexpr float kTcLog2e = 1.4426950408889634f;
+
+// mbarriers
+enum {
+    kBarQ = 0,          // queries written (128 arrivals)
+    kBarKvFull = 1,     // [2] tile decoded (128 arrivals)
+    kBarKvEmpty = 3,    // [2] tile's MMAs done (commit)
+    kBarSFull = 5,      // [2] scores ready (commit)
+    kBarSFree = 7,      // [2] scores read (128 arrivals)
+    kBarPFull = 9,      // P written, O rescaled (128 arrivals)
+    kBarPvDone = 10,    // P V of a tile done (commit)
+    kBarDrain = 11,     // every MMA of the CTA done (commit), before TMEM is released
+    kBarCount = 12
+};
+
+struct TcParams {
+    CacheView kc, vc;
+    const __half *q;        // [n_q][Hq][128] fp16
+    float *out;             // [n_q][Hq][128] fp32
+    int64_t pos0, n_q;
+    int32_t seq, n_q_heads, group, bq;
+    int32_t chunked_k, chunked_v;
+    float score_scale;      // softmax scale * log2(e) / sqrt(128)
+};
+
+struct TcSmem {
+    alignas(1024) uint8_t q[32768];        // Q~ [row][coord], K-major
+    alignas(1024) uint8_t k[2][32768];     // K tile [key][coord], K-major
+    alignas(1024) uint8_t v[2][32768];     // V tile [key][coord], coords contiguous (MN-major)
+    alignas(1024) uint8_t p[32768];        // P [row][key], K-major
+    alignas(16) uint8_t raw[2][kTcKeys * kTcSlot];   // staged blocks of one tile: K, V
+    alignas(16) uint8_t raw_pad[16];
+    float kn[2][kTcKeys], vn[2][kTcKeys];
+    uint8_t ok[2][kTcKeys];                // [K/V][key] row present
+    alignas(8) uint64_t bar[kBarCount];
+    uint32_t tmem;
+};
+
+// Byte offset of element (r, c) of a 128-column tile in the no-swizzle canonical layout with
+// rows along M/N (8-row groups 2048 bytes apart) and columns along K (8-column groups 128
+// bytes apart).
+__device__ __forceinline__ uint32_t canon(int r, int c) {
+    return (uint32_t)((r >> 3) * 2048 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
+// The MN-major V tile: keys are K (8-key groups 2048 bytes apart), coords are N (8-coord
+// groups 128 bytes apart), coords contiguous inside a core matrix.
+__device__ __forceinline__ uint32_t canon_mn(int key, int c) {
+    return (uint32_t)((c >> 3) * 128 + (key >> 3) * 2048 + (key & 7) * 16 + (c & 7) * 2);
+}
+
+// Shared-memory matrix descriptor (no swizzle): start, leading (K) and stride (M/N) byte
+// offsets in 16-byte units, descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B, M = 128, N = 128.
+constexpr uint32_t idesc_f16(bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&r)[32]) {
+    uint32_t u[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]),
+          "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]),
+          "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]),
+          "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __uint_as_float(u[i]);
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(__float_as_uint(r[0])), "r"(__float_as_uint(r[1])),
+          "r"(__float_as_uint(r[2])), "r"(__float_as_uint(r[3])), "r"(__float_as_uint(r[4])),
+          "r"(__float_as_uint(r[5])), "r"(__float_as_uint(r[6])), "r"(__float_as_uint(r[7])),
+          "r"(__float_as_uint(r[8])), "r"(__float_as_uint(r[9])), "r"(__float_as_uint(r[10])),
+          "r"(__float_as_uint(r[11])), "r"(__float_as_uint(r[12])), "r"(__float_as_uint(r[13])),
+          "r"(__float_as_uint(r[14])), "r"(__float_as_uint(r[15])), "r"(__float_as_uint(r[16])),
+          "r"(__float_as_uint(r[17])), "r"(__float_as_uint(r[18])), "r"(__float_as_uint(r[19])),
+          "r"(__float_as_uint(r[20])), "r"(__float_as_uint(r[21])), "r"(__float_as_uint(r[22])),
+          "r"(__float_as_uint(r[23])), "r"(__float_as_uint(r[24])), "r"(__float_as_uint(r[25])),
+          "r"(__float_as_uint(r[26])), "r"(__float_as_uint(r[27])), "r"(__float_as_uint(r[28])),
+          "r"(__float_as_uint(r[29])), "r"(__float_as_uint(r[30])), "r"(__float_as_uint(r[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_bar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void tc_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Bounded wait on a phase; false (and TQ_ERR_DEVICE_TIMEOUT recorded) on timeout.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kTcWaitLimit; ++it) {
+        uint32_t ok;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}\n"
+                     : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+        if (ok) return true;
+    }
+    record_error(TQ_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Producer thread pt stages key pt of tile [t0, t0+128) of both caches: the 16-byte chunks
+// covering head g's block (rows of 16-byte multiples, cp.async), else the block's 2-byte
+// words with plain loads; the block lands at (block offset in the row) mod 16 of its slot.
+template <int TK, int TV>
+__device__ __forceinline__ void tc_stage(const TcParams &p, TcSmem &sm, int g, int64_t t0,
+                                         int64_t n_keys, int pt) {
+    const int64_t t = t0 + pt;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const CacheView &cv = i == 0 ? p.kc : p.vc;
+        const uint8_t *row = t < n_keys ? row_ptr(cv, p.seq, t) : nullptr;
+        const int bb = i == 0 ? block_bytes(TK) : block_bytes(TV);
+        const int bo = g * bb, c0 = bo & ~15, end = (bo + bb + 15) & ~15;
+        uint8_t *slot = sm.raw[i] + pt * kTcSlot;
+        if (row) {
+            if (i == 0 ? p.chunked_k : p.chunked_v) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (c0 + 16 * c < end) cp_async16(smem_u32(slot + 16 * c), row + c0 + 16 * c);
+            } else {
+                const uint16_t *src = reinterpret_cast<const uint16_t *>(row + bo);
+                uint16_t *dst = reinterpret_cast<uint16_t *>(slot + (bo - c0));
+                for (int w = 0; w < bb / 2; ++w) dst[w] = src[w];
+            }
+        }
+        sm.ok[i][pt] = row ? 1 : 0;
+    }
+}
+
+// Producer thread pt decodes key pt of the staged tile of one cache into fp16 centroid
+// values at tile[key][coord] (K-major, or MN-major for V) and its norm (0 if absent).
+template <int TYPE, bool MN>
+__device__ __forceinline__ void tc_decode(const uint8_t *raw, const uint8_t *ok, int g,
+                                          const HalfTables &tab, uint8_t *tile, float *norm,
+                                          int pt) {
+    constexpr int B = block_bytes(TYPE);
+    const uint8_t *slot = raw + pt * kTcSlot;
+    const int off = (g * B) & 15;
+    const Shifts sh = {2u, 4u, 1u << 16, 1u << 30, 1u << 31};
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const Quarter<TYPE> qw = load_quarter<TYPE>(slot, (off + 2 + 8 * q4) & ~3,
+                                                    (off + 34 + 4 * q4) & ~3,
+                                                    (uint32_t)((off + 2) & 3) * 8u);
+#pragma unroll
+        for (int ww = 0; ww < 2; ++ww)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                uint32_t o[4];
+                group_pairs<TYPE>(qw, ww, r, tab, sh, o);
+                const int c0 = 32 * q4 + 16 * ww + 8 * r;
+                *reinterpret_cast<uint4 *>(tile + (MN ? canon_mn(pt, c0) : canon(pt, c0))) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            }
+    }
+    norm[pt] = ok[pt] ? ld_norm(slot + off) : 0.f;
+}
+
+// In-thread Walsh-Hadamard butterflies over 128 values, h = 1 .. 64.
+__device__ __forceinline__ void fwht128(float (&x)[128]) {
+#pragma unroll
+    for (int h = 1; h < 128; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+            if (!(i & h)) {
+                const float a = x[i], b = x[i + h];
+                x[i] = a + b;
+                x[i + h] = a - b;
+            }
+}
+
+template <int TK, int TV>
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    extern __shared__ __align__(16) uint8_t smem_raw[];   // 16: the runtime guarantees no more
+    // the MMA operand tiles must start on a 1024-byte boundary of the shared window (the
+    // dynamic block itself may start after static shared memory at a lower alignment)
+    TcSmem &sm = *reinterpret_cast<TcSmem *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = blockIdx.y, G = p.group, Hq = p.n_q_heads;
+    const int64_t j0 = (int64_t)blockIdx.x * p.bq;
+    const int64_t j_end = min64(p.n_q, j0 + p.bq);
+    const int64_t n_keys = p.pos0 + j_end;                  // rows the CTA's last query sees
+    const int n_tiles = (int)((n_keys + kTcKeys - 1) / kTcKeys);
+    auto bar = [&](int i) { return smem_u32(&sm.bar[i]); };
+
+    if (tid == 0) {
+        abort_flag = 0;
+        tc_bar_init(bar(kBarQ), kTcSoftmax);
+        for (int b = 0; b < 2; ++b) {
+            tc_bar_init(bar(kBarKvFull + b), kTcProducer);
+            tc_bar_init(bar(kBarKvEmpty + b), 1);
+            tc_bar_init(bar(kBarSFull + b), 1);
+            tc_bar_init(bar(kBarSFree + b), kTcSoftmax);
+        }
+        tc_bar_init(bar(kBarPFull), kTcSoftmax);
+        tc_bar_init(bar(kBarPvDone), 1);
+        tc_bar_init(bar(kBarDrain), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 8) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&sm.tmem)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    volatile int *abort_v = &abort_flag;
+
+    if (warp < 4) {
+        // ================= softmax: thread r owns row r = TMEM lane r
+        const int r = tid, jl = r / G, hl = r - jl * G;
+        const bool valid = jl < p.bq && j0 + jl < p.n_q;
+        const int64_t qpos = valid ? p.pos0 + j0 + jl : INT64_MAX;
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        {
+            float x[128];
+            if (valid) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    p.q + ((j0 + jl) * Hq + g * G + hl) * (int64_t)kBlock);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 u = src[c];
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+                        x[8 * c + 2 * e] = f.x;
+                        x[8 * c + 2 * e + 1] = f.y;
+                    }
+                }
+                if (p.kc.has_signs) {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(__float_as_uint(x[i]) ^ sign_mask(p.kc, i));
+                }
+                fwht128(x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) x[i] = 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack_half2(x[8 * c + 2 * e] * p.score_scale, x[8 * c + 2 * e + 1] * p.score_scale);
+                *reinterpret_cast<uint4 *>(sm.q + canon(r, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_arrive(bar(kBarQ));
+
+        float m_run = -INFINITY, l_run = 0.f;
+        // every thread runs every tile (the TMEM loads are warp-collective); after a timeout
+        // the remaining waits are skipped
+        for (int i = 0; i < n_tiles; ++i) {
+            const int b = i & 1;
+            if (!*abort_v && !tc_wait(bar(kBarSFull + b), (uint32_t)((i >> 1) & 1))) *abort_v = 1;
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float t[32];
+                tc_ld32(tmem + lane_base + 128u * b + 32u * c, t);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[32 * c + e] = t[e];
+            }
+            tc_fence_before();
+            tc_arrive(bar(kBarSFree + b));
+            const int64_t t0 = (int64_t)i * kTcKeys;
+            float mx = m_run;
+#pragma unroll
+            for (int j = 0; j < 128; ++j) {
+                const float v = s[j] * sm.kn[b][j];
+                s[j] = t0 + j > qpos ? -INFINITY : v;
+                mx = fmaxf(mx, s[j]);
+            }
+            const float alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
+            m_run = mx;
+            if (i > 0) {
+                if (!*abort_v && !tc_wait(bar(kBarPvDone), (uint32_t)((i - 1) & 1))) *abort_v = 1;
+                tc_fence_after();
+            }
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 8 * c + 2 * e;
+                    const float p0 = mx == -INFINITY ? 0.f : ex2(s[j] - mx);
+                    const float p1 = mx == -INFINITY ? 0.f : ex2(s[j + 1] - mx);
+                    psum += p0 + p1;
+                    w[e] = pack_half2(p0 * sm.vn[b][j], p1 * sm.vn[b][j + 1]);
+                }
+                *reinterpret_cast<uint4 *>(sm.p + canon(r, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l_run = l_run * alpha + psum;
+            if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float t[32];
+                    tc_ld32(tmem + lane_base + 256u + 32u * c, t);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) t[e] *= alpha;
+                    tc_st32(tmem + lane_base + 256u + 32u * c, t);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            tc_arrive(bar(kBarPFull));
+        }
+        // ---- epilogue: O / l, inverse rotation of the row, V signs, store
+        bool done = n_tiles > 0 && !*abort_v &&
+                    tc_wait(bar(kBarPvDone), (uint32_t)((n_tiles - 1) & 1));
+        tc_fence_after();
+        float o[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float t[32];
+            tc_ld32(tmem + lane_base + 256u + 32u * c, t);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[32 * c + e] = t[e];
+        }
+        if (valid && done) {
+            const float inv = l_run > 0.f ? kInvSqrt128 / l_run : 0.f;
+            fwht128(o);
+            float4 *dst = reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)kBlock);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float v4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v4[e] = __uint_as_float(__float_as_uint(o[4 * c + e] * inv) ^ sign_mask(p.vc, 4 * c + e));
+                dst[c] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+            }
+        }
+    } else if (warp < 8) {
+        // ================= producers: stage and decode key tiles
+        const int pt = tid - kTcSoftmax;
+        const HalfTables tk = make_tables<TK>(), tv = make_tables<TV>();
+        if (n_tiles > 0) tc_stage<TK, TV>(p, sm, g, 0, n_keys, pt);
+        cp_async_commit();
+        for (int i = 0; i < n_tiles; ++i) {   // the same trip count for all producers (bar.sync)
+            const int b = i & 1;
+            cp_async_wait<0>();
+            named_sync(1, kTcProducer);   // the whole tile has landed
+            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarKvEmpty + b), (uint32_t)(((i - 2) >> 1) & 1)))
+                *abort_v = 1;
+            tc_decode<TK, false>(sm.raw[0], sm.ok[0], g, tk, sm.k[b], sm.kn[b], pt);
+            tc_decode<TV, true>(sm.raw[1], sm.ok[1], g, tv, sm.v[b], sm.vn[b], pt);
+            named_sync(1, kTcProducer);   // everyone is done with the staged bytes
+            if (i + 1 < n_tiles) tc_stage<TK, TV>(p, sm, g, (int64_t)(i + 1) * kTcKeys, n_keys, pt);
+            cp_async_commit();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_arrive(bar(kBarKvFull + b));
+        }
+        cp_async_wait<0>();
+    } else if (lane == 0) {
+        // ================= MMA issue (one thread)
+        constexpr uint32_t idesc_s = idesc_f16(false), idesc_pv = idesc_f16(true);
+        const uint32_t q_base = smem_u32(sm.q), p_base = smem_u32(sm.p);
+        bool ok = tc_wait(bar(kBarQ), 0);
+        auto issue_s = [&](int i) {
+            const int b = i & 1;
+            ok = ok && tc_wait(bar(kBarKvFull + b), (uint32_t)((i >> 1) & 1));
+            if (i >= 2) ok = ok && tc_wait(bar(kBarSFree + b), (uint32_t)(((i - 2) >> 1) & 1));
+            if (!ok) return;
+            tc_fence_after();
+            const uint32_t k_base = smem_u32(sm.k[b]);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc_mma(tmem + 128u * b, sdesc(q_base + 256u * ks, 128, 2048),
+                       sdesc(k_base + 256u * ks, 128, 2048), idesc_s, ks > 0);
+            tc_commit(bar(kBarSFull + b));
+        };
+        if (n_tiles > 0) issue_s(0);
+        for (int i = 0; i < n_tiles && ok; ++i) {
+            if (i + 1 < n_tiles) issue_s(i + 1);
+            ok = ok && tc_wait(bar(kBarPFull), (uint32_t)(i & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t v_base = smem_u32(sm.v[i & 1]);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc_mma(tmem + 256u, sdesc(p_base + 256u * kk, 128, 2048),
+                       sdesc(v_base + 4096u * kk, 2048, 128), idesc_pv, (i > 0 || kk > 0));
+            tc_commit(bar(kBarPvDone));
+            tc_commit(bar(kBarKvEmpty + (i & 1)));
+        }
+        if (!ok) *abort_v = 1;
+        tc_commit(bar(kBarDrain));   // arrives once everything issued above has completed
+        tc_wait(bar(kBarDrain), 0);
+    }
+    // teardown: every MMA has completed (the softmax waited for the last P V, or all roles
+    // gave up on a timeout); release the tensor memory
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 8)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+template <int TK, int TV>
+tq_status launch_tc_t(const TcParams &p, unsigned grid_x, unsigned n_kv_heads, cudaStream_t stream) {
+    const size_t smem = sizeof(TcSmem) + 1024;   // room to align the tiles to 1024 bytes
+    if (cudaFuncSetAttribute(prefill_tc_kernel<TK, TV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return TQ_ERR_CUDA;
+    PdlConfig lc(dim3(grid_x, n_kv_heads), dim3(kTcThreads), smem, stream);
+    return check_cuda(cudaLaunchKernelEx(&lc.cfg, prefill_tc_kernel<TK, TV>, p));
+}
+
+}  // namespace
+
+tq_status launch_prefill_tc(const tq_cache &k, const tq_cache &v, const void *q, int32_t seq_id,
+                            int64_t pos0, int64_t n_q, int n_q_heads, float scale, float *out,
+                            cudaStream_t stream) {
+    TcParams p;
+    p.kc = make_view(k);
+    p.vc = make_view(v);
+    p.q = static_cast<const __half *>(q);
+    p.out = out;
+    p.pos0 = pos0;
+    p.n_q = n_q;
+    p.seq = seq_id;
+    p.n_q_heads = n_q_heads;
+    p.group = n_q_heads / k.n_kv_heads;
+    p.bq = kTcRows / p.group;
+    p.chunked_k = p.kc.row_bytes % 16 == 0;
+    p.chunked_v = p.vc.row_bytes % 16 == 0;
+    p.score_scale = scale * kTcLog2e * kInvSqrt128;
+    const int64_t grid_x = (n_q + p.bq - 1) / p.bq;
+    if (grid_x > 0x7fffffff) return TQ_ERR_UNSUPPORTED;
+    const unsigned gx = (unsigned)grid_x, hk = (unsigned)k.n_kv_heads;
+    if (k.type == TQ_TURBO3 && v.type == TQ_TURBO3) return launch_tc_t<3, 3>(p, gx, hk, stream);
+    if (k.type == TQ_TURBO2 && v.type == TQ_TURBO2) return launch_tc_t<2, 2>(p, gx, hk, stream);
+    if (k.type == TQ_TURBO3 && v.type == TQ_TURBO2) return launch_tc_t<3, 2>(p, gx, hk, stream);
+    return launch_tc_t<2, 3>(p, gx, hk, stream);
+}
+
+}  // namespace tq
