@@ -36,7 +36,6 @@ constexpr int kTcKeys = 128;          // keys per tile
 constexpr int kTcSoftmax = 128;       // threads of warps 0-3
 constexpr int kTcProducer = 128;      // threads of warps 4-7
 constexpr int kTcThreads = kTcSoftmax + kTcProducer + 32;
-constexpr int kTcSlot = 64;           // staged bytes per key and cache
 constexpr uint32_t kTcWaitLimit = 1u << 20;
 constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256,384)
 constexpr float kTcLog2e = 1.4426950408889634f;
@@ -69,9 +68,8 @@ struct TcSmem {
     alignas(1024) uint8_t k[2][32768];     // K tile [key][coord], K-major
     alignas(1024) uint8_t v[2][32768];     // V tile [key][coord], coords contiguous (MN-major)
     alignas(1024) uint8_t p[32768];        // P [row][key], K-major
-    alignas(16) uint8_t raw[2][kTcKeys * kTcSlot];   // staged blocks of one tile: K, V
-    alignas(16) uint8_t raw_pad[16];
-    float kn[2][kTcKeys], vn[2][kTcKeys];
+    alignas(16) uint8_t raw[2][kTcKeys * 64];   // staged blocks of one tile (K, V), word-major
+    float kn[2][kTcKeys];                  // K norms of the two tile buffers
     uint8_t ok[2][kTcKeys];                // [K/V][key] row present
     alignas(8) uint64_t bar[kBarCount];
     uint32_t tmem;
@@ -172,9 +170,20 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Producer thread pt stages key pt of tile [t0, t0+128) of both caches: the 16-byte chunks
-// covering head g's block (rows of 16-byte multiples, cp.async), else the block's 2-byte
-// words with plain loads; the block lands at (block offset in the row) mod 16 of its slot.
+// Staged tile bytes are word-major: logical word j (4 bytes) of key k sits at word
+// j * 128 + k of the cache's staging area, so that the decode threads (one per key) read
+// the same logical word of 32 consecutive keys from 32 different banks.  Logical byte 0 is
+// the first byte of the 4-byte word holding the block's first byte; the block starts at
+// logical byte (block offset in the row) mod 4.
+constexpr int kTcWords = 16;   // logical words staged per key (covers 50 bytes at any offset)
+
+__device__ __forceinline__ uint32_t wm_word(const uint32_t *raw, int j, int pt) {
+    return raw[j * kTcKeys + pt];
+}
+
+// Producer thread pt stages key pt of tile [t0, t0+128) of both caches: the 4-byte words
+// covering head g's block with cp.async when rows are 16-byte multiples (so words are
+// aligned), else the block's 2-byte halves with plain loads.
 template <int TK, int TV>
 __device__ __forceinline__ void tc_stage(const TcParams &p, TcSmem &sm, int g, int64_t t0,
                                          int64_t n_keys, int pt) {
@@ -184,50 +193,76 @@ __device__ __forceinline__ void tc_stage(const TcParams &p, TcSmem &sm, int g, i
         const CacheView &cv = i == 0 ? p.kc : p.vc;
         const uint8_t *row = t < n_keys ? row_ptr(cv, p.seq, t) : nullptr;
         const int bb = i == 0 ? block_bytes(TK) : block_bytes(TV);
-        const int bo = g * bb, c0 = bo & ~15, end = (bo + bb + 15) & ~15;
-        uint8_t *slot = sm.raw[i] + pt * kTcSlot;
+        const int bo = g * bb, w0 = bo >> 2, nw = ((bo + bb + 3) >> 2) - w0;
+        uint32_t *raw = reinterpret_cast<uint32_t *>(sm.raw[i]);
         if (row) {
             if (i == 0 ? p.chunked_k : p.chunked_v) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (c0 + 16 * c < end) cp_async16(smem_u32(slot + 16 * c), row + c0 + 16 * c);
+                for (int j = 0; j < nw; ++j)
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n"
+                                 ::"r"(smem_u32(raw + j * kTcKeys + pt)),
+                                   "l"(row + 4 * (w0 + j)) : "memory");
             } else {
+                // 2-byte aligned rows: halves h of the block go to logical byte (bo & 3) + 2h
                 const uint16_t *src = reinterpret_cast<const uint16_t *>(row + bo);
-                uint16_t *dst = reinterpret_cast<uint16_t *>(slot + (bo - c0));
-                for (int w = 0; w < bb / 2; ++w) dst[w] = src[w];
+                uint16_t *dst = reinterpret_cast<uint16_t *>(raw);
+                for (int h = 0; h < bb / 2; ++h) {
+                    const int lb = (bo & 3) + 2 * h;   // logical byte
+                    dst[2 * ((lb >> 2) * kTcKeys + pt) + ((lb >> 1) & 1)] = src[h];
+                }
             }
         }
         sm.ok[i][pt] = row ? 1 : 0;
     }
 }
 
-// Producer thread pt decodes key pt of the staged tile of one cache into fp16 centroid
-// values at tile[key][coord] (K-major, or MN-major for V) and its norm (0 if absent).
+// Producer thread pt decodes key pt of the staged tile of one cache: K into fp16 centroids
+// at tile[key][coord] (K-major) and its norm into norm[key]; V into fp16 |v| c (MN-major).
+// Absent rows get norm 0.
 template <int TYPE, bool MN>
-__device__ __forceinline__ void tc_decode(const uint8_t *raw, const uint8_t *ok, int g,
+__device__ __forceinline__ void tc_decode(const uint8_t *raw_bytes, const uint8_t *ok, int g,
                                           const HalfTables &tab, uint8_t *tile, float *norm,
                                           int pt) {
     constexpr int B = block_bytes(TYPE);
-    const uint8_t *slot = raw + pt * kTcSlot;
-    const int off = (g * B) & 15;
-    const Shifts sh = {2u, 4u, 1u << 16, 1u << 30, 1u << 31};
+    const uint32_t *raw = reinterpret_cast<const uint32_t *>(raw_bytes);
+    const int off = (g * B) & 3;               // the block's first logical byte
+    const uint32_t sh = (uint32_t)((off + 2) & 3) * 8u;
+    const Shifts shifts = {2u, 4u, 1u << 16, 1u << 30, 1u << 31};
+    // the norm: 2 bytes at logical byte off (off is even, so they share a word), 0 for an
+    // absent row.  V folds it into the tile values (|v| c); K keeps it apart (norm[]) and
+    // the scores are scaled in fp32, which keeps one fp16 rounding on the score path
+    const uint32_t w0 = wm_word(raw, 0, pt);
+    const __half nrm = ok[pt] ? __ushort_as_half((uint16_t)(w0 >> (8 * off))) : __ushort_as_half(0);
+    const __half2 n2 = __halves2half2(nrm, nrm);
+    if (!MN) norm[pt] = __half2float(nrm);
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
-        const Quarter<TYPE> qw = load_quarter<TYPE>(slot, (off + 2 + 8 * q4) & ~3,
-                                                    (off + 34 + 4 * q4) & ~3,
-                                                    (uint32_t)((off + 2) & 3) * 8u);
+        // the quarter's low-plane bytes start at logical byte off + 2 + 8 q4, its
+        // high-plane word at off + 34 + 4 q4 (word-aligned reads, then funnel shifts)
+        const int jw = (off + 2 + 8 * q4) >> 2, jv = (off + 34 + 4 * q4) >> 2;
+        Quarter<TYPE> qw;
+        const uint32_t a = wm_word(raw, jw, pt), b = wm_word(raw, jw + 1, pt), c = wm_word(raw, jw + 2, pt);
+        qw.W0 = __funnelshift_r(a, b, sh);
+        qw.W1 = __funnelshift_r(b, c, sh);
+        if (TYPE == TQ_TURBO3) qw.V = __funnelshift_r(wm_word(raw, jv, pt), wm_word(raw, jv + 1, pt), sh);
+        else qw.V = 0u;
 #pragma unroll
         for (int ww = 0; ww < 2; ++ww)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 uint32_t o[4];
-                group_pairs<TYPE>(qw, ww, r, tab, sh, o);
+                group_pairs<TYPE>(qw, ww, r, tab, shifts, o);
+                if (MN) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        __half2 h = __hmul2(*reinterpret_cast<const __half2 *>(&o[e]), n2);
+                        o[e] = *reinterpret_cast<const uint32_t *>(&h);
+                    }
+                }
                 const int c0 = 32 * q4 + 16 * ww + 8 * r;
                 *reinterpret_cast<uint4 *>(tile + (MN ? canon_mn(pt, c0) : canon(pt, c0))) =
                     make_uint4(o[0], o[1], o[2], o[3]);
             }
     }
-    norm[pt] = ok[pt] ? ld_norm(slot + off) : 0.f;
 }
 
 // In-thread Walsh-Hadamard butterflies over 128 values, h = 1 .. 64.
@@ -346,33 +381,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
             tc_fence_before();
             tc_arrive(bar(kBarSFree + b));
             const int64_t t0 = (int64_t)i * kTcKeys;
-            float mx = m_run;
+            // keys past this row's position are masked; eight partial maxima keep the
+            // dependency chains short (one softmax warp per scheduler hides little latency)
+            const int lim = (int)max64(-1, min64(qpos - t0, kTcKeys));   // keys j > lim are masked
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = m_run;
 #pragma unroll
             for (int j = 0; j < 128; ++j) {
-                const float v = s[j] * sm.kn[b][j];
-                s[j] = t0 + j > qpos ? -INFINITY : v;
-                mx = fmaxf(mx, s[j]);
+                s[j] = j > lim ? -INFINITY : s[j] * sm.kn[b][j];
+                mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
             }
-            const float alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
-            m_run = mx;
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            // lazy rescaling: the reference maximum moves only when the row's maximum exceeds
+            // it by more than 8 (log2 units), so p <= 2^8 (fp16-safe: |v| is in the V tile) and
+            // O in tensor memory is rarely rewritten
+            float alpha = 1.f;
+            if (m_run == -INFINITY || mx > m_run + 8.f) {
+                alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
+                m_run = mx;
+            }
             if (i > 0) {
                 if (!*abort_v && !tc_wait(bar(kBarPvDone), (uint32_t)((i - 1) & 1))) *abort_v = 1;
                 tc_fence_after();
             }
-            float psum = 0.f;
+            float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float mref = m_run == -INFINITY ? 0.f : m_run;   // all masked: every p is 0
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int j = 8 * c + 2 * e;
-                    const float p0 = mx == -INFINITY ? 0.f : ex2(s[j] - mx);
-                    const float p1 = mx == -INFINITY ? 0.f : ex2(s[j + 1] - mx);
-                    psum += p0 + p1;
-                    w[e] = pack_half2(p0 * sm.vn[b][j], p1 * sm.vn[b][j + 1]);
+                    const float p0 = ex2(s[j] - mref), p1 = ex2(s[j + 1] - mref);
+                    ps8[2 * e] += p0;
+                    ps8[2 * e + 1] += p1;
+                    w[e] = pack_half2(p0, p1);
                 }
                 *reinterpret_cast<uint4 *>(sm.p + canon(r, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
+            const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
             l_run = l_run * alpha + psum;
             if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -427,7 +476,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
             if (i >= 2 && !*abort_v && !tc_wait(bar(kBarKvEmpty + b), (uint32_t)(((i - 2) >> 1) & 1)))
                 *abort_v = 1;
             tc_decode<TK, false>(sm.raw[0], sm.ok[0], g, tk, sm.k[b], sm.kn[b], pt);
-            tc_decode<TV, true>(sm.raw[1], sm.ok[1], g, tv, sm.v[b], sm.vn[b], pt);
+            tc_decode<TV, true>(sm.raw[1], sm.ok[1], g, tv, sm.v[b], nullptr, pt);
             named_sync(1, kTcProducer);   // everyone is done with the staged bytes
             if (i + 1 < n_tiles) tc_stage<TK, TV>(p, sm, g, (int64_t)(i + 1) * kTcKeys, n_keys, pt);
             cp_async_commit();
