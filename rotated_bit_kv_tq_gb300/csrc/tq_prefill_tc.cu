@@ -37,20 +37,22 @@ constexpr int kTcSoftmax = 128;       // threads of warps 0-3
 constexpr int kTcProducer = 128;      // threads of warps 4-7
 constexpr int kTcThreads = kTcSoftmax + kTcProducer + 32;
 constexpr uint32_t kTcWaitLimit = 1u << 20;
+constexpr uint32_t kTcPollLimit = 1u << 24;   // polls without progress of the MMA thread
 constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256,384)
 constexpr float kTcLog2e = 1.4426950408889634f;
 
 // mbarriers
 enum {
     kBarQ = 0,          // queries written (128 arrivals)
-    kBarKvFull = 1,     // [2] tile decoded (128 arrivals)
-    kBarKvEmpty = 3,    // [2] tile's MMAs done (commit)
-    kBarSFull = 5,      // [2] scores ready (commit)
-    kBarSFree = 7,      // [2] scores read (128 arrivals)
-    kBarPFull = 9,      // P written, O rescaled (128 arrivals)
-    kBarPvDone = 10,    // P V of a tile done (commit)
-    kBarDrain = 11,     // every MMA of the CTA done (commit), before TMEM is released
-    kBarCount = 12
+    kBarKFull = 1,      // [2] K tile and its norms decoded (128 arrivals)
+    kBarVFull = 3,      // [2] V tile decoded (128 arrivals)
+    kBarVEmpty = 5,     // [2] the tile's P V done (commit)
+    kBarSFull = 7,      // [2] scores ready (commit)
+    kBarSFree = 9,      // [2] scores and K norms read (128 arrivals); implies the S MMAs are done
+    kBarPFull = 11,     // P written, O rescaled (128 arrivals)
+    kBarPvDone = 12,    // P V of a tile done (commit)
+    kBarDrain = 13,     // every MMA of the CTA done (commit), before TMEM is released
+    kBarCount = 14
 };
 
 struct TcParams {
@@ -153,6 +155,14 @@ __device__ __forceinline__ void tc_bar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void tc_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool tc_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}\n"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
 }
 // Bounded wait on a phase; false (and TQ_ERR_DEVICE_TIMEOUT recorded) on timeout.
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity) {
@@ -299,8 +309,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         abort_flag = 0;
         tc_bar_init(bar(kBarQ), kTcSoftmax);
         for (int b = 0; b < 2; ++b) {
-            tc_bar_init(bar(kBarKvFull + b), kTcProducer);
-            tc_bar_init(bar(kBarKvEmpty + b), 1);
+            tc_bar_init(bar(kBarKFull + b), kTcProducer);
+            tc_bar_init(bar(kBarVFull + b), kTcProducer);
+            tc_bar_init(bar(kBarVEmpty + b), 1);
             tc_bar_init(bar(kBarSFull + b), 1);
             tc_bar_init(bar(kBarSFree + b), kTcSoftmax);
         }
@@ -378,8 +389,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
 #pragma unroll
                 for (int e = 0; e < 32; ++e) s[32 * c + e] = t[e];
             }
-            tc_fence_before();
-            tc_arrive(bar(kBarSFree + b));
             const int64_t t0 = (int64_t)i * kTcKeys;
             // keys past this row's position are masked; eight partial maxima keep the
             // dependency chains short (one softmax warp per scheduler hides little latency)
@@ -392,6 +401,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
                 s[j] = j > lim ? -INFINITY : s[j] * sm.kn[b][j];
                 mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
             }
+            // S buffer b and the K norms of tile buffer b are free for tile i + 2
+            tc_fence_before();
+            tc_arrive(bar(kBarSFree + b));
             const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             // lazy rescaling: the reference maximum moves only when the row's maximum exceeds
@@ -473,15 +485,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
             const int b = i & 1;
             cp_async_wait<0>();
             named_sync(1, kTcProducer);   // the whole tile has landed
-            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarKvEmpty + b), (uint32_t)(((i - 2) >> 1) & 1)))
-                *abort_v = 1;
+            const uint32_t ph = (uint32_t)(((i - 2) >> 1) & 1);
+            // K tile b is free once the softmax has read tile i - 2's scores and norms (its S
+            // MMAs are then done); V tile b once tile i - 2's P V is done
+            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarSFree + b), ph)) *abort_v = 1;
             tc_decode<TK, false>(sm.raw[0], sm.ok[0], g, tk, sm.k[b], sm.kn[b], pt);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_arrive(bar(kBarKFull + b));
+            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarVEmpty + b), ph)) *abort_v = 1;
             tc_decode<TV, true>(sm.raw[1], sm.ok[1], g, tv, sm.v[b], nullptr, pt);
             named_sync(1, kTcProducer);   // everyone is done with the staged bytes
             if (i + 1 < n_tiles) tc_stage<TK, TV>(p, sm, g, (int64_t)(i + 1) * kTcKeys, n_keys, pt);
             cp_async_commit();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_arrive(bar(kBarKvFull + b));
+            tc_arrive(bar(kBarVFull + b));
         }
         cp_async_wait<0>();
     } else if (lane == 0) {
@@ -489,32 +506,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         constexpr uint32_t idesc_s = idesc_f16(false), idesc_pv = idesc_f16(true);
         const uint32_t q_base = smem_u32(sm.q), p_base = smem_u32(sm.p);
         bool ok = tc_wait(bar(kBarQ), 0);
-        auto issue_s = [&](int i) {
-            const int b = i & 1;
-            ok = ok && tc_wait(bar(kBarKvFull + b), (uint32_t)((i >> 1) & 1));
-            if (i >= 2) ok = ok && tc_wait(bar(kBarSFree + b), (uint32_t)(((i - 2) >> 1) & 1));
-            if (!ok) return;
-            tc_fence_after();
-            const uint32_t k_base = smem_u32(sm.k[b]);
+        // issue S(ns) and P V(npv) in whichever order their inputs become ready: S(i + 1)
+        // must not hold back P V(i) while tile i + 1 is still being decoded
+        int ns = 0, npv = 0;
+        uint32_t idle = 0;
+        while (ok && npv < n_tiles) {
+            bool progressed = false;
+            if (ns < n_tiles) {
+                const int b = ns & 1;
+                if (tc_test(bar(kBarKFull + b), (uint32_t)((ns >> 1) & 1)) &&
+                    (ns < 2 || tc_test(bar(kBarSFree + b), (uint32_t)(((ns - 2) >> 1) & 1)))) {
+                    tc_fence_after();
+                    const uint32_t k_base = smem_u32(sm.k[b]);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc_mma(tmem + 128u * b, sdesc(q_base + 256u * ks, 128, 2048),
-                       sdesc(k_base + 256u * ks, 128, 2048), idesc_s, ks > 0);
-            tc_commit(bar(kBarSFull + b));
-        };
-        if (n_tiles > 0) issue_s(0);
-        for (int i = 0; i < n_tiles && ok; ++i) {
-            if (i + 1 < n_tiles) issue_s(i + 1);
-            ok = ok && tc_wait(bar(kBarPFull), (uint32_t)(i & 1));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t v_base = smem_u32(sm.v[i & 1]);
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc_mma(tmem + 128u * b, sdesc(q_base + 256u * ks, 128, 2048),
+                               sdesc(k_base + 256u * ks, 128, 2048), idesc_s, ks > 0);
+                    tc_commit(bar(kBarSFull + b));
+                    ++ns;
+                    progressed = true;
+                }
+            }
+            if (npv < ns && tc_test(bar(kBarPFull), (uint32_t)(npv & 1)) &&
+                tc_test(bar(kBarVFull + (npv & 1)), (uint32_t)((npv >> 1) & 1))) {
+                tc_fence_after();
+                const uint32_t v_base = smem_u32(sm.v[npv & 1]);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc_mma(tmem + 256u, sdesc(p_base + 256u * kk, 128, 2048),
-                       sdesc(v_base + 4096u * kk, 2048, 128), idesc_pv, (i > 0 || kk > 0));
-            tc_commit(bar(kBarPvDone));
-            tc_commit(bar(kBarKvEmpty + (i & 1)));
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma(tmem + 256u, sdesc(p_base + 256u * kk, 128, 2048),
+                           sdesc(v_base + 4096u * kk, 2048, 128), idesc_pv, (npv > 0 || kk > 0));
+                tc_commit(bar(kBarPvDone));
+                tc_commit(bar(kBarVEmpty + (npv & 1)));
+                ++npv;
+                progressed = true;
+            }
+            if (progressed) idle = 0;
+            else if (++idle > kTcPollLimit || *abort_v) {
+                if (!*abort_v) record_error(TQ_ERR_DEVICE_TIMEOUT);
+                ok = false;
+            }
         }
         if (!ok) *abort_v = 1;
         tc_commit(bar(kBarDrain));   // arrives once everything issued above has completed
