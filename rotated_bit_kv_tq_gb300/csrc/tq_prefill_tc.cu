@@ -38,19 +38,25 @@ constexpr int kTcProducer = 128;      // threads of warps 4-7
 constexpr int kTcThreads = kTcSoftmax + kTcProducer + 32;
 constexpr uint32_t kTcWaitLimit = 1u << 20;
 constexpr uint32_t kTcPollLimit = 1u << 24;   // polls without progress of the MMA thread
-constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256,384)
+// tensor memory columns: S0 [0,128), S1 [128,256), O [256,384) fp32; P0 [384,448),
+// P1 [448,512) fp16 pairs (the A operand of P V)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 256, kTmemP = 384;
 constexpr float kTcLog2e = 1.4426950408889634f;
 
 // mbarriers
+// Buffer b of a double-buffered resource serves tiles b, b + 2, ...; a waiter for tile i
+// waits for phase i >> 1 of barrier b, which is safe because no barrier can run more than
+// one phase ahead of (or behind) its waiters: each role waits for the previous use of a
+// buffer before it arrives for the next.
 enum {
     kBarQ = 0,          // queries written (128 arrivals)
     kBarKFull = 1,      // [2] K tile and its norms decoded (128 arrivals)
     kBarVFull = 3,      // [2] V tile decoded (128 arrivals)
-    kBarVEmpty = 5,     // [2] the tile's P V done (commit)
+    kBarPvFree = 5,     // [2] the tile's P V done: V tile and P buffer free (commit)
     kBarSFull = 7,      // [2] scores ready (commit)
     kBarSFree = 9,      // [2] scores and K norms read (128 arrivals); implies the S MMAs are done
-    kBarPFull = 11,     // P written, O rescaled (128 arrivals)
-    kBarPvDone = 12,    // P V of a tile done (commit)
+    kBarPFull = 11,     // [2] P written, O rescaled (128 arrivals)
     kBarDrain = 13,     // every MMA of the CTA done (commit), before TMEM is released
     kBarCount = 14
 };
@@ -69,7 +75,6 @@ struct TcSmem {
     alignas(1024) uint8_t q[32768];        // Q~ [row][coord], K-major
     alignas(1024) uint8_t k[2][32768];     // K tile [key][coord], K-major
     alignas(1024) uint8_t v[2][32768];     // V tile [key][coord], coords contiguous (MN-major)
-    alignas(1024) uint8_t p[32768];        // P [row][key], K-major
     alignas(16) uint8_t raw[2][kTcKeys * 64];   // staged blocks of one tile (K, V), word-major
     float kn[2][kTcKeys];                  // K norms of the two tile buffers
     uint8_t ok[2][kTcKeys];                // [K/V][key] row present
@@ -105,6 +110,13 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
                  ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+// The same with A read from tensor memory (row m = lane m, two fp16 K values per column).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -311,12 +323,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         for (int b = 0; b < 2; ++b) {
             tc_bar_init(bar(kBarKFull + b), kTcProducer);
             tc_bar_init(bar(kBarVFull + b), kTcProducer);
-            tc_bar_init(bar(kBarVEmpty + b), 1);
+            tc_bar_init(bar(kBarPvFree + b), 1);
+            tc_bar_init(bar(kBarPFull + b), kTcSoftmax);
             tc_bar_init(bar(kBarSFull + b), 1);
             tc_bar_init(bar(kBarSFree + b), kTcSoftmax);
         }
-        tc_bar_init(bar(kBarPFull), kTcSoftmax);
-        tc_bar_init(bar(kBarPvDone), 1);
         tc_bar_init(bar(kBarDrain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -414,51 +425,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
                 alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
                 m_run = mx;
             }
-            if (i > 0) {
-                if (!*abort_v && !tc_wait(bar(kBarPvDone), (uint32_t)((i - 1) & 1))) *abort_v = 1;
-                tc_fence_after();
-            }
+            // P buffer b is free once tile i - 2's P V is done
+            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarPvFree + b), (uint32_t)(((i - 2) >> 1) & 1)))
+                *abort_v = 1;
+            tc_fence_after();
             float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             const float mref = m_run == -INFINITY ? 0.f : m_run;   // all masked: every p is 0
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint32_t w[4];
+            for (int c = 0; c < 2; ++c) {
+                float w[32];   // 32 columns of fp16 pairs (keys 64 c + 2 e, + 1)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = 8 * c + 2 * e;
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 64 * c + 2 * e;
                     const float p0 = ex2(s[j] - mref), p1 = ex2(s[j + 1] - mref);
-                    ps8[2 * e] += p0;
-                    ps8[2 * e + 1] += p1;
-                    w[e] = pack_half2(p0, p1);
+                    ps8[(2 * e) & 7] += p0;
+                    ps8[(2 * e + 1) & 7] += p1;
+                    w[e] = __uint_as_float(pack_half2(p0, p1));
                 }
-                *reinterpret_cast<uint4 *>(sm.p + canon(r, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                tc_st32(tmem + lane_base + kTmemP + 64u * b + 32u * c, w);
             }
             const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
             l_run = l_run * alpha + psum;
             if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // the running output must hold every P V up to tile i - 1 before it is scaled
+                if (!*abort_v && !tc_wait(bar(kBarPvFree + ((i - 1) & 1)), (uint32_t)(((i - 1) >> 1) & 1)))
+                    *abort_v = 1;
+                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float t[32];
-                    tc_ld32(tmem + lane_base + 256u + 32u * c, t);
+                    tc_ld32(tmem + lane_base + kTmemO + 32u * c, t);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) t[e] *= alpha;
-                    tc_st32(tmem + lane_base + 256u + 32u * c, t);
+                    tc_st32(tmem + lane_base + kTmemO + 32u * c, t);
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
-            tc_arrive(bar(kBarPFull));
+            tc_arrive(bar(kBarPFull + b));
         }
         // ---- epilogue: O / l, inverse rotation of the row, V signs, store
         bool done = n_tiles > 0 && !*abort_v &&
-                    tc_wait(bar(kBarPvDone), (uint32_t)((n_tiles - 1) & 1));
+                    tc_wait(bar(kBarPvFree + ((n_tiles - 1) & 1)), (uint32_t)(((n_tiles - 1) >> 1) & 1));
         tc_fence_after();
         float o[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             float t[32];
-            tc_ld32(tmem + lane_base + 256u + 32u * c, t);
+            tc_ld32(tmem + lane_base + kTmemO + 32u * c, t);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[32 * c + e] = t[e];
         }
@@ -492,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
             tc_decode<TK, false>(sm.raw[0], sm.ok[0], g, tk, sm.k[b], sm.kn[b], pt);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_arrive(bar(kBarKFull + b));
-            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarVEmpty + b), ph)) *abort_v = 1;
+            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarPvFree + b), ph)) *abort_v = 1;
             tc_decode<TV, true>(sm.raw[1], sm.ok[1], g, tv, sm.v[b], nullptr, pt);
             named_sync(1, kTcProducer);   // everyone is done with the staged bytes
             if (i + 1 < n_tiles) tc_stage<TK, TV>(p, sm, g, (int64_t)(i + 1) * kTcKeys, n_keys, pt);
@@ -504,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
     } else if (lane == 0) {
         // ================= MMA issue (one thread)
         constexpr uint32_t idesc_s = idesc_f16(false), idesc_pv = idesc_f16(true);
-        const uint32_t q_base = smem_u32(sm.q), p_base = smem_u32(sm.p);
+        const uint32_t q_base = smem_u32(sm.q);
         bool ok = tc_wait(bar(kBarQ), 0);
         // issue S(ns) and P V(npv) in whichever order their inputs become ready: S(i + 1)
         // must not hold back P V(i) while tile i + 1 is still being decoded
@@ -527,16 +541,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
                     progressed = true;
                 }
             }
-            if (npv < ns && tc_test(bar(kBarPFull), (uint32_t)(npv & 1)) &&
+            if (npv < ns && tc_test(bar(kBarPFull + (npv & 1)), (uint32_t)((npv >> 1) & 1)) &&
                 tc_test(bar(kBarVFull + (npv & 1)), (uint32_t)((npv >> 1) & 1))) {
                 tc_fence_after();
-                const uint32_t v_base = smem_u32(sm.v[npv & 1]);
+                const int b = npv & 1;
+                const uint32_t v_base = smem_u32(sm.v[b]);
+                // A = P from tensor memory (16 keys = 8 columns per MMA), B = the V tile
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma(tmem + 256u, sdesc(p_base + 256u * kk, 128, 2048),
-                           sdesc(v_base + 4096u * kk, 2048, 128), idesc_pv, (npv > 0 || kk > 0));
-                tc_commit(bar(kBarPvDone));
-                tc_commit(bar(kBarVEmpty + (npv & 1)));
+                    tc_mma_ts(tmem + kTmemO, tmem + kTmemP + 64u * b + 8u * kk,
+                              sdesc(v_base + 4096u * kk, 2048, 128), idesc_pv, (npv > 0 || kk > 0));
+                tc_commit(bar(kBarPvFree + b));
                 ++npv;
                 progressed = true;
             }
