@@ -5,18 +5,21 @@
 // compressed cache, dequantisation inside the attention tiles; TinyLLaMA article, section 7:
 // the query at position N attends to rows 0..N).  The work split follows the roles the
 // tensor-memory model suggests:
-//  - warps 0-3 (one thread per row of the 128-row tile, row = TMEM lane): rotate the queries
-//    into shared memory; per key tile read the scores S from TMEM, scale by |k|, mask, run
-//    the online softmax entirely inside the thread, write P (times |v|, fp16) to shared
-//    memory, rescale O in TMEM when the running maximum moved; at the end read O, divide,
-//    inverse-FWHT the row in registers and store it;
-//  - warps 4-7: stage each tile's block bytes (cp.async), decode them once into fp16
-//    centroid values laid out as the MMA operands (K: keys x coords, K-major; V: keys x
-//    coords with coords contiguous, MN-major), double-buffered;
-//  - warp 8: allocates TMEM and issues the MMAs from one thread: S[b] = Q~ K^T (M = 128
-//    rows, N = 128 keys, K = 128 coords) into one of two TMEM score buffers, so the scores
-//    of the next tile are computed while the softmax works on this one, and
-//    O += P V (N = 128 coords, K = 128 keys); completions arrive on mbarriers through
+//  - warps 0-7, two threads per row of the 128-row tile (row = TMEM lane, warps q and q + 4
+//    share lanes 32q..32q+31), each thread owning 64 of a tile's 128 keys: rotate the
+//    queries into shared memory; per key tile read the scores S from TMEM, scale by |k|,
+//    mask on the diagonal tiles, exchange the row maximum with the partner thread, write P
+//    (fp16) into tensor memory, rescale O there when the running maximum moved; at the
+//    end read O, divide, inverse-FWHT the row (the last butterfly across the pair) and
+//    store it;
+//  - warps 8-11 (K) and 12-15 (V), one thread per key: stage the tile's block bytes
+//    (cp.async) and decode them once into fp16 values laid out as the MMA operands (K:
+//    centroids, keys x coords, K-major, norms apart; V: |v| times centroids, keys x coords
+//    with coords contiguous, MN-major), double-buffered;
+//  - warp 16: allocates TMEM and issues the MMAs from one thread, in whichever order their
+//    inputs become ready: S[b] = Q~ K^T (M = 128 rows, N = 128 keys, K = 128 coords) into
+//    one of two TMEM score buffers, and O += P V with P read from one of two TMEM buffers
+//    (N = 128 coords, K = 128 keys); completions arrive on mbarriers through
 //    tcgen05.commit.
 // Shared-memory operands use the no-swizzle canonical layout: 8 x 16-byte core matrices,
 // core matrices adjacent along K 128 bytes apart (LBO), 8-row groups along M/N 2048 bytes
@@ -33,8 +36,10 @@ namespace {
 
 constexpr int kTcRows = 128;          // (query token, head) rows per CTA = TMEM lanes
 constexpr int kTcKeys = 128;          // keys per tile
-constexpr int kTcSoftmax = 128;       // threads of warps 0-3
-constexpr int kTcProducer = 128;      // threads of warps 4-7
+constexpr int kTcSoftmax = 256;       // warps 0-7: two threads per row (one per 64-key half)
+constexpr int kTcGroup = 128;         // threads of one producer group (warps 8-11 K, 12-15 V)
+constexpr int kTcProducer = 2 * kTcGroup;
+constexpr int kTcMmaWarp = (kTcSoftmax + kTcProducer) / 32;
 constexpr int kTcThreads = kTcSoftmax + kTcProducer + 32;
 constexpr uint32_t kTcWaitLimit = 1u << 20;
 constexpr uint32_t kTcPollLimit = 1u << 24;   // polls without progress of the MMA thread
@@ -77,6 +82,7 @@ struct TcSmem {
     alignas(1024) uint8_t v[2][32768];     // V tile [key][coord], coords contiguous (MN-major)
     alignas(16) uint8_t raw[2][kTcKeys * 64];   // staged blocks of one tile (K, V), word-major
     float kn[2][kTcKeys];                  // K norms of the two tile buffers
+    float xch[2][2][kTcRows];              // [tile parity][half][row] row maxima, then sums
     uint8_t ok[2][kTcKeys];                // [K/V][key] row present
     alignas(8) uint64_t bar[kBarCount];
     uint32_t tmem;
@@ -162,6 +168,33 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&r)[32]) {
         : "memory");
 }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane (two loads, one wait, in one
+// statement so that no use of the values can be scheduled before the wait).
+__device__ __forceinline__ void tc_ld64(uint32_t taddr, float (&r)[64]) {
+    uint32_t u[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,"
+        "%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]),
+          "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]),
+          "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]),
+          "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31]),
+          "=r"(u[32]), "=r"(u[33]), "=r"(u[34]), "=r"(u[35]), "=r"(u[36]), "=r"(u[37]),
+          "=r"(u[38]), "=r"(u[39]), "=r"(u[40]), "=r"(u[41]), "=r"(u[42]), "=r"(u[43]),
+          "=r"(u[44]), "=r"(u[45]), "=r"(u[46]), "=r"(u[47]), "=r"(u[48]), "=r"(u[49]),
+          "=r"(u[50]), "=r"(u[51]), "=r"(u[52]), "=r"(u[53]), "=r"(u[54]), "=r"(u[55]),
+          "=r"(u[56]), "=r"(u[57]), "=r"(u[58]), "=r"(u[59]), "=r"(u[60]), "=r"(u[61]),
+          "=r"(u[62]), "=r"(u[63])
+        : "r"(taddr), "r"(taddr + 32u)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) r[i] = __uint_as_float(u[i]);
+}
+
 __device__ __forceinline__ void tc_bar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -203,38 +236,34 @@ __device__ __forceinline__ uint32_t wm_word(const uint32_t *raw, int j, int pt) 
     return raw[j * kTcKeys + pt];
 }
 
-// Producer thread pt stages key pt of tile [t0, t0+128) of both caches: the 4-byte words
-// covering head g's block with cp.async when rows are 16-byte multiples (so words are
-// aligned), else the block's 2-byte halves with plain loads.
-template <int TK, int TV>
-__device__ __forceinline__ void tc_stage(const TcParams &p, TcSmem &sm, int g, int64_t t0,
+// Producer thread pt of a group stages key pt of tile [t0, t0+128) of its cache: the
+// 4-byte words covering head g's block with cp.async when rows are 16-byte multiples (so
+// words are aligned), else the block's 2-byte halves with plain loads.
+template <int TYPE>
+__device__ __forceinline__ void tc_stage(const CacheView &cv, int32_t seq, bool chunked,
+                                         uint8_t *raw_bytes, uint8_t *ok, int g, int64_t t0,
                                          int64_t n_keys, int pt) {
     const int64_t t = t0 + pt;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const CacheView &cv = i == 0 ? p.kc : p.vc;
-        const uint8_t *row = t < n_keys ? row_ptr(cv, p.seq, t) : nullptr;
-        const int bb = i == 0 ? block_bytes(TK) : block_bytes(TV);
-        const int bo = g * bb, w0 = bo >> 2, nw = ((bo + bb + 3) >> 2) - w0;
-        uint32_t *raw = reinterpret_cast<uint32_t *>(sm.raw[i]);
-        if (row) {
-            if (i == 0 ? p.chunked_k : p.chunked_v) {
-                for (int j = 0; j < nw; ++j)
-                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n"
-                                 ::"r"(smem_u32(raw + j * kTcKeys + pt)),
-                                   "l"(row + 4 * (w0 + j)) : "memory");
-            } else {
-                // 2-byte aligned rows: halves h of the block go to logical byte (bo & 3) + 2h
-                const uint16_t *src = reinterpret_cast<const uint16_t *>(row + bo);
-                uint16_t *dst = reinterpret_cast<uint16_t *>(raw);
-                for (int h = 0; h < bb / 2; ++h) {
-                    const int lb = (bo & 3) + 2 * h;   // logical byte
-                    dst[2 * ((lb >> 2) * kTcKeys + pt) + ((lb >> 1) & 1)] = src[h];
-                }
+    const uint8_t *row = t < n_keys ? row_ptr(cv, seq, t) : nullptr;
+    constexpr int bb = block_bytes(TYPE);
+    const int bo = g * bb, w0 = bo >> 2, nw = ((bo + bb + 3) >> 2) - w0;
+    uint32_t *raw = reinterpret_cast<uint32_t *>(raw_bytes);
+    if (row) {
+        if (chunked) {
+            for (int j = 0; j < nw; ++j)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n"
+                             ::"r"(smem_u32(raw + j * kTcKeys + pt)), "l"(row + 4 * (w0 + j)) : "memory");
+        } else {
+            // 2-byte aligned rows: halves h of the block go to logical byte (bo & 3) + 2h
+            const uint16_t *src = reinterpret_cast<const uint16_t *>(row + bo);
+            uint16_t *dst = reinterpret_cast<uint16_t *>(raw);
+            for (int h = 0; h < bb / 2; ++h) {
+                const int lb = (bo & 3) + 2 * h;   // logical byte
+                dst[2 * ((lb >> 2) * kTcKeys + pt) + ((lb >> 1) & 1)] = src[h];
             }
         }
-        sm.ok[i][pt] = row ? 1 : 0;
     }
+    ok[pt] = row ? 1 : 0;
 }
 
 // Producer thread pt decodes key pt of the staged tile of one cache: K into fp16 centroids
@@ -287,17 +316,49 @@ __device__ __forceinline__ void tc_decode(const uint8_t *raw_bytes, const uint8_
     }
 }
 
-// In-thread Walsh-Hadamard butterflies over 128 values, h = 1 .. 64.
-__device__ __forceinline__ void fwht128(float (&x)[128]) {
+// In-thread Walsh-Hadamard butterflies over 64 values, h = 1 .. 32.
+__device__ __forceinline__ void fwht64(float (&x)[64]) {
 #pragma unroll
-    for (int h = 1; h < 128; h <<= 1)
+    for (int h = 1; h < 64; h <<= 1)
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
             if (!(i & h)) {
                 const float a = x[i], b = x[i + h];
                 x[i] = a + b;
                 x[i + h] = a - b;
             }
+}
+
+// One producer group: stage and decode every tile of its cache (K: centroids and norms;
+// V: |v| c), double-buffered.  Each thread reads back only the words it staged itself, so
+// the group needs no barrier of its own; tile buffer b is rewritten once the consumers of
+// tile i - 2 are done with it (K: the softmax has read that tile's scores and norms; V: its
+// P V has completed).
+template <int TYPE, bool IS_V>
+__device__ __forceinline__ void tc_produce(const TcParams &p, TcSmem &sm, int g, int64_t n_keys,
+                                           int n_tiles, int pt, volatile int *abort_v) {
+    const CacheView &cv = IS_V ? p.vc : p.kc;
+    const bool chunked = IS_V ? p.chunked_v : p.chunked_k;
+    uint8_t *raw = sm.raw[IS_V ? 1 : 0];
+    uint8_t *ok = sm.ok[IS_V ? 1 : 0];
+    const HalfTables tab = make_tables<TYPE>();
+    const int free_bar = IS_V ? kBarPvFree : kBarSFree, full_bar = IS_V ? kBarVFull : kBarKFull;
+    if (n_tiles > 0) tc_stage<TYPE>(cv, p.seq, chunked, raw, ok, g, 0, n_keys, pt);
+    cp_async_commit();
+    for (int i = 0; i < n_tiles; ++i) {
+        const int b = i & 1;
+        cp_async_wait<0>();   // this thread's words of tile i have landed
+        if (i >= 2 && !*abort_v &&
+            !tc_wait(smem_u32(&sm.bar[free_bar + b]), (uint32_t)(((i - 2) >> 1) & 1)))
+            *abort_v = 1;
+        if (IS_V) tc_decode<TYPE, true>(raw, ok, g, tab, sm.v[b], nullptr, pt);
+        else tc_decode<TYPE, false>(raw, ok, g, tab, sm.k[b], sm.kn[b], pt);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_arrive(smem_u32(&sm.bar[full_bar + b]));
+        if (i + 1 < n_tiles) tc_stage<TYPE>(cv, p.seq, chunked, raw, ok, g, (int64_t)(i + 1) * kTcKeys, n_keys, pt);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
 }
 
 template <int TK, int TV>
@@ -314,6 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
     const int64_t j0 = (int64_t)blockIdx.x * p.bq;
     const int64_t j_end = min64(p.n_q, j0 + p.bq);
     const int64_t n_keys = p.pos0 + j_end;                  // rows the CTA's last query sees
+    const int64_t first_pos = p.pos0 + j0;                  // the CTA's first query position
     const int n_tiles = (int)((n_keys + kTcKeys - 1) / kTcKeys);
     auto bar = [&](int i) { return smem_u32(&sm.bar[i]); };
 
@@ -321,8 +383,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         abort_flag = 0;
         tc_bar_init(bar(kBarQ), kTcSoftmax);
         for (int b = 0; b < 2; ++b) {
-            tc_bar_init(bar(kBarKFull + b), kTcProducer);
-            tc_bar_init(bar(kBarVFull + b), kTcProducer);
+            tc_bar_init(bar(kBarKFull + b), kTcGroup);
+            tc_bar_init(bar(kBarVFull + b), kTcGroup);
             tc_bar_init(bar(kBarPvFree + b), 1);
             tc_bar_init(bar(kBarPFull + b), kTcSoftmax);
             tc_bar_init(bar(kBarSFull + b), 1);
@@ -331,7 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         tc_bar_init(bar(kBarDrain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 8) {
+    if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(&sm.tmem)), "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -342,84 +404,102 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
     const uint32_t tmem = sm.tmem;
     volatile int *abort_v = &abort_flag;
 
-    if (warp < 4) {
-        // ================= softmax: thread r owns row r = TMEM lane r
-        const int r = tid, jl = r / G, hl = r - jl * G;
+    if (warp < kTcSoftmax / 32) {
+        // ================= softmax: thread (r, h) owns keys 64 h .. 64 h + 63 of every tile
+        // for row r = TMEM lane r (warps quad and quad + 4 share the lanes of quad)
+        const int quad = warp & 3, h = warp >> 2;
+        const int r = 32 * quad + lane, jl = r / G, hl = r - jl * G;
         const bool valid = jl < p.bq && j0 + jl < p.n_q;
         const int64_t qpos = valid ? p.pos0 + j0 + jl : INT64_MAX;
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+        const uint32_t pair_bar = 3u + (uint32_t)quad;   // named barrier of the row's two threads
         {
-            float x[128];
+            // coords 64 h .. 64 h + 63 of Q~ = H (D q) * scale: the stride-64 butterfly straight
+            // from the loaded row, then strides 1 .. 32 inside the thread
+            float x[64];
             if (valid) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(
                     p.q + ((j0 + jl) * Hq + g * G + hl) * (int64_t)kBlock);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 u = src[c];
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 ua = src[c], ub = src[c + 8];   // coords 8 c .. and 64 + 8 c ..
+                    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-                        x[8 * c + 2 * e] = f.x;
-                        x[8 * c + 2 * e + 1] = f.y;
+                        const int i0 = 8 * c + 2 * e;
+                        const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&wa[e]));
+                        const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&wb[e]));
+                        float a0 = fa.x, a1 = fa.y, b0 = fb.x, b1 = fb.y;
+                        if (p.kc.has_signs) {
+                            a0 = __uint_as_float(__float_as_uint(a0) ^ sign_mask(p.kc, i0));
+                            a1 = __uint_as_float(__float_as_uint(a1) ^ sign_mask(p.kc, i0 + 1));
+                            b0 = __uint_as_float(__float_as_uint(b0) ^ sign_mask(p.kc, 64 + i0));
+                            b1 = __uint_as_float(__float_as_uint(b1) ^ sign_mask(p.kc, 64 + i0 + 1));
+                        }
+                        x[i0] = h ? a0 - b0 : a0 + b0;
+                        x[i0 + 1] = h ? a1 - b1 : a1 + b1;
                     }
                 }
-                if (p.kc.has_signs) {
-#pragma unroll
-                    for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(__float_as_uint(x[i]) ^ sign_mask(p.kc, i));
-                }
-                fwht128(x);
+                fwht64(x);
             } else {
 #pragma unroll
-                for (int i = 0; i < 128; ++i) x[i] = 0.f;
+                for (int i = 0; i < 64; ++i) x[i] = 0.f;
             }
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     w[e] = pack_half2(x[8 * c + 2 * e] * p.score_scale, x[8 * c + 2 * e + 1] * p.score_scale);
-                *reinterpret_cast<uint4 *>(sm.q + canon(r, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(sm.q + canon(r, 64 * h + 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_arrive(bar(kBarQ));
 
-        float m_run = -INFINITY, l_run = 0.f;
-        // every thread runs every tile (the TMEM loads are warp-collective); after a timeout
-        // the remaining waits are skipped
+        float m_run = -INFINITY, l_run = 0.f;   // l_run: this half's share of the row sum
+        // every thread runs every tile (the TMEM accesses and the pair barrier are
+        // collective); after a timeout the remaining waits are skipped
         for (int i = 0; i < n_tiles; ++i) {
             const int b = i & 1;
             if (!*abort_v && !tc_wait(bar(kBarSFull + b), (uint32_t)((i >> 1) & 1))) *abort_v = 1;
             tc_fence_after();
-            float s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float t[32];
-                tc_ld32(tmem + lane_base + 128u * b + 32u * c, t);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) s[32 * c + e] = t[e];
-            }
-            const int64_t t0 = (int64_t)i * kTcKeys;
-            // keys past this row's position are masked; eight partial maxima keep the
-            // dependency chains short (one softmax warp per scheduler hides little latency)
-            const int lim = (int)max64(-1, min64(qpos - t0, kTcKeys));   // keys j > lim are masked
+            float s[64];
+            tc_ld64(tmem + lane_base + 128u * b + 64u * h, s);
+            const float *kn = sm.kn[b] + 64 * h;
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = m_run;
+            if ((int64_t)i * kTcKeys + (kTcKeys - 1) <= first_pos) {
+                // every key of the tile is visible to every row of the CTA
 #pragma unroll
-            for (int j = 0; j < 128; ++j) {
-                s[j] = j > lim ? -INFINITY : s[j] * sm.kn[b][j];
-                mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
+                for (int j = 0; j < 64; ++j) {
+                    s[j] *= kn[j];
+                    mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
+                }
+            } else {
+                // keys past this row's position are masked
+                const int64_t t0 = (int64_t)i * kTcKeys + 64 * h;
+                const int lim = (int)max64(-1, min64(qpos - t0, 64));   // keys j > lim are masked
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    s[j] = j > lim ? -INFINITY : s[j] * kn[j];
+                    mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
+                }
             }
             // S buffer b and the K norms of tile buffer b are free for tile i + 2
             tc_fence_before();
             tc_arrive(bar(kBarSFree + b));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            // the row's maximum over both halves (exchange slot b is reused two tiles on,
+            // after the partner has passed the next pair barrier)
+            sm.xch[b][h][r] = mx;
+            named_sync(pair_bar, 64);
+            mx = fmaxf(mx, sm.xch[b][h ^ 1][r]);
             // lazy rescaling: the reference maximum moves only when the row's maximum exceeds
             // it by more than 8 (log2 units), so p <= 2^8 (fp16-safe: |v| is in the V tile) and
-            // O in tensor memory is rarely rewritten
+            // O in tensor memory is rarely rewritten; both halves take the same decisions
             float alpha = 1.f;
             if (m_run == -INFINITY || mx > m_run + 8.f) {
                 alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
@@ -431,33 +511,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
             tc_fence_after();
             float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             const float mref = m_run == -INFINITY ? 0.f : m_run;   // all masked: every p is 0
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float w[32];   // 32 columns of fp16 pairs (keys 64 c + 2 e, + 1)
+            {
+                float w[32];   // columns 32 h + e hold the fp16 pair of keys 64 h + 2 e, + 1
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int j = 64 * c + 2 * e;
-                    const float p0 = ex2(s[j] - mref), p1 = ex2(s[j + 1] - mref);
+                    const float p0 = ex2(s[2 * e] - mref), p1 = ex2(s[2 * e + 1] - mref);
                     ps8[(2 * e) & 7] += p0;
                     ps8[(2 * e + 1) & 7] += p1;
                     w[e] = __uint_as_float(pack_half2(p0, p1));
                 }
-                tc_st32(tmem + lane_base + kTmemP + 64u * b + 32u * c, w);
+                tc_st32(tmem + lane_base + kTmemP + 64u * b + 32u * h, w);
             }
             const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
             l_run = l_run * alpha + psum;
             if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // the running output must hold every P V up to tile i - 1 before it is scaled
+                // the running output must hold every P V up to tile i - 1 before it is scaled;
+                // this half scales output columns 64 h .. 64 h + 63
                 if (!*abort_v && !tc_wait(bar(kBarPvFree + ((i - 1) & 1)), (uint32_t)(((i - 1) >> 1) & 1)))
                     *abort_v = 1;
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     float t[32];
-                    tc_ld32(tmem + lane_base + kTmemO + 32u * c, t);
+                    tc_ld32(tmem + lane_base + kTmemO + 64u * h + 32u * c, t);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) t[e] *= alpha;
-                    tc_st32(tmem + lane_base + kTmemO + 32u * c, t);
+                    tc_st32(tmem + lane_base + kTmemO + 64u * h + 32u * c, t);
                 }
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -465,56 +544,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
             tc_arrive(bar(kBarPFull + b));
         }
         // ---- epilogue: O / l, inverse rotation of the row, V signs, store
-        bool done = n_tiles > 0 && !*abort_v &&
-                    tc_wait(bar(kBarPvFree + ((n_tiles - 1) & 1)), (uint32_t)(((n_tiles - 1) >> 1) & 1));
+        const bool done = n_tiles > 0 && !*abort_v &&
+                          tc_wait(bar(kBarPvFree + ((n_tiles - 1) & 1)), (uint32_t)(((n_tiles - 1) >> 1) & 1));
         tc_fence_after();
-        float o[128];
+        sm.xch[n_tiles & 1][h][r] = l_run;   // slot of tile n_tiles - 2: the partner is past it
+        float o[64];
+        tc_ld64(tmem + lane_base + kTmemO + 64u * h, o);
+        fwht64(o);   // strides 1 .. 32 of this half
+        // the stride-64 butterfly pairs coord c with c + 64: the halves swap through the K
+        // tile area, idle once every MMA has completed (float4 chunks XOR-swizzled by row)
+        float *xo = reinterpret_cast<float *>(sm.k[0]);
+        auto xo_at = [&](int row, int c4) { return xo + row * 128 + (((c4 ^ row) & 31) << 2); };
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float t[32];
-            tc_ld32(tmem + lane_base + kTmemO + 32u * c, t);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[32 * c + e] = t[e];
-        }
+        for (int c = 0; c < 16; ++c)
+            *reinterpret_cast<float4 *>(xo_at(r, 16 * h + c)) =
+                make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        named_sync(pair_bar, 64);
+        const float l_row = l_run + sm.xch[n_tiles & 1][h ^ 1][r];
         if (valid && done) {
-            const float inv = l_run > 0.f ? kInvSqrt128 / l_run : 0.f;
-            fwht128(o);
-            float4 *dst = reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)kBlock);
+            const float inv = l_row > 0.f ? kInvSqrt128 / l_row : 0.f;
+            float4 *dst = reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)kBlock + 64 * h);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 16; ++c) {
+                const float4 u = *reinterpret_cast<const float4 *>(xo_at(r, 16 * (h ^ 1) + c));
+                const float pv[4] = {u.x, u.y, u.z, u.w};
                 float v4[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    v4[e] = __uint_as_float(__float_as_uint(o[4 * c + e] * inv) ^ sign_mask(p.vc, 4 * c + e));
+                for (int e = 0; e < 4; ++e) {
+                    // h = 0: coord c' = o + partner (coords c', c' + 64); h = 1: partner - o
+                    const float y = h ? pv[e] - o[4 * c + e] : o[4 * c + e] + pv[e];
+                    v4[e] = __uint_as_float(__float_as_uint(y * inv) ^ sign_mask(p.vc, 64 * h + 4 * c + e));
+                }
                 dst[c] = make_float4(v4[0], v4[1], v4[2], v4[3]);
             }
         }
-    } else if (warp < 8) {
-        // ================= producers: stage and decode key tiles
-        const int pt = tid - kTcSoftmax;
-        const HalfTables tk = make_tables<TK>(), tv = make_tables<TV>();
-        if (n_tiles > 0) tc_stage<TK, TV>(p, sm, g, 0, n_keys, pt);
-        cp_async_commit();
-        for (int i = 0; i < n_tiles; ++i) {   // the same trip count for all producers (bar.sync)
-            const int b = i & 1;
-            cp_async_wait<0>();
-            named_sync(1, kTcProducer);   // the whole tile has landed
-            const uint32_t ph = (uint32_t)(((i - 2) >> 1) & 1);
-            // K tile b is free once the softmax has read tile i - 2's scores and norms (its S
-            // MMAs are then done); V tile b once tile i - 2's P V is done
-            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarSFree + b), ph)) *abort_v = 1;
-            tc_decode<TK, false>(sm.raw[0], sm.ok[0], g, tk, sm.k[b], sm.kn[b], pt);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_arrive(bar(kBarKFull + b));
-            if (i >= 2 && !*abort_v && !tc_wait(bar(kBarPvFree + b), ph)) *abort_v = 1;
-            tc_decode<TV, true>(sm.raw[1], sm.ok[1], g, tv, sm.v[b], nullptr, pt);
-            named_sync(1, kTcProducer);   // everyone is done with the staged bytes
-            if (i + 1 < n_tiles) tc_stage<TK, TV>(p, sm, g, (int64_t)(i + 1) * kTcKeys, n_keys, pt);
-            cp_async_commit();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_arrive(bar(kBarVFull + b));
-        }
-        cp_async_wait<0>();
+    } else if (warp < kTcMmaWarp) {
+        // ================= producers: warps 8-11 the K cache, 12-15 the V cache
+        const int pt = (tid - kTcSoftmax) & (kTcGroup - 1);
+        if (tid - kTcSoftmax < kTcGroup) tc_produce<TK, false>(p, sm, g, n_keys, n_tiles, pt, abort_v);
+        else tc_produce<TV, true>(p, sm, g, n_keys, n_tiles, pt, abort_v);
     } else if (lane == 0) {
         // ================= MMA issue (one thread)
         constexpr uint32_t idesc_s = idesc_f16(false), idesc_pv = idesc_f16(true);
@@ -570,7 +638,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 8)
+    if (warp == kTcMmaWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
