@@ -72,6 +72,8 @@ struct TcParams {
     float *out;             // [n_q][Hq][128] fp32
     int64_t pos0, n_q;
     int32_t seq, n_q_heads, group, bq;
+    int32_t n_kv_heads;
+    int64_t n_qblocks;      // query blocks of bq tokens
     int32_t chunked_k, chunked_v;
     float score_scale;      // softmax scale * log2(e) / sqrt(128)
 };
@@ -371,8 +373,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
     TcSmem &sm = *reinterpret_cast<TcSmem *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     __shared__ int abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.y, G = p.group, Hq = p.n_q_heads;
-    const int64_t j0 = (int64_t)blockIdx.x * p.bq;
+    // CTAs run longest first: the last query block (the most keys) of every head first
+    const int g = (int)(blockIdx.x % (unsigned)p.n_kv_heads), G = p.group, Hq = p.n_q_heads;
+    const int64_t j0 = (p.n_qblocks - 1 - (int64_t)(blockIdx.x / (unsigned)p.n_kv_heads)) * p.bq;
     const int64_t j_end = min64(p.n_q, j0 + p.bq);
     const int64_t n_keys = p.pos0 + j_end;                  // rows the CTA's last query sees
     const int64_t first_pos = p.pos0 + j0;                  // the CTA's first query position
@@ -643,12 +646,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
 }
 
 template <int TK, int TV>
-tq_status launch_tc_t(const TcParams &p, unsigned grid_x, unsigned n_kv_heads, cudaStream_t stream) {
+tq_status launch_tc_t(const TcParams &p, unsigned n_ctas, cudaStream_t stream) {
     const size_t smem = sizeof(TcSmem) + 1024;   // room to align the tiles to 1024 bytes
     if (cudaFuncSetAttribute(prefill_tc_kernel<TK, TV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return TQ_ERR_CUDA;
-    PdlConfig lc(dim3(grid_x, n_kv_heads), dim3(kTcThreads), smem, stream);
+    PdlConfig lc(dim3(n_ctas), dim3(kTcThreads), smem, stream);
     return check_cuda(cudaLaunchKernelEx(&lc.cfg, prefill_tc_kernel<TK, TV>, p));
 }
 
@@ -671,13 +674,15 @@ tq_status launch_prefill_tc(const tq_cache &k, const tq_cache &v, const void *q,
     p.chunked_k = p.kc.row_bytes % 16 == 0;
     p.chunked_v = p.vc.row_bytes % 16 == 0;
     p.score_scale = scale * kTcLog2e * kInvSqrt128;
-    const int64_t grid_x = (n_q + p.bq - 1) / p.bq;
-    if (grid_x > 0x7fffffff) return TQ_ERR_UNSUPPORTED;
-    const unsigned gx = (unsigned)grid_x, hk = (unsigned)k.n_kv_heads;
-    if (k.type == TQ_TURBO3 && v.type == TQ_TURBO3) return launch_tc_t<3, 3>(p, gx, hk, stream);
-    if (k.type == TQ_TURBO2 && v.type == TQ_TURBO2) return launch_tc_t<2, 2>(p, gx, hk, stream);
-    if (k.type == TQ_TURBO3 && v.type == TQ_TURBO2) return launch_tc_t<3, 2>(p, gx, hk, stream);
-    return launch_tc_t<2, 3>(p, gx, hk, stream);
+    p.n_kv_heads = k.n_kv_heads;
+    p.n_qblocks = (n_q + p.bq - 1) / p.bq;
+    const int64_t n_ctas = p.n_qblocks * k.n_kv_heads;
+    if (n_ctas > 0x7fffffff) return TQ_ERR_UNSUPPORTED;
+    const unsigned nc = (unsigned)n_ctas;
+    if (k.type == TQ_TURBO3 && v.type == TQ_TURBO3) return launch_tc_t<3, 3>(p, nc, stream);
+    if (k.type == TQ_TURBO2 && v.type == TQ_TURBO2) return launch_tc_t<2, 2>(p, nc, stream);
+    if (k.type == TQ_TURBO3 && v.type == TQ_TURBO2) return launch_tc_t<3, 2>(p, nc, stream);
+    return launch_tc_t<2, 3>(p, nc, stream);
 }
 
 }  // namespace tq
