@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--kernel-probe", type=int, default=0, metavar="CTX",
                     help="time one layer's encode and attention at context CTX (the small "
                          "case the ncu captures use) instead of the full benchmark")
+    ap.add_argument("--prefill-probe", type=int, default=0, metavar="CTX",
+                    help="time one layer's prompt attention over a whole CTX-token prompt "
+                         "(one chunk from position 0; the small case of the prefill capture)")
     return ap.parse_args()
 
 
@@ -540,10 +543,46 @@ def kernel_probe(args):
                       "attn_gbs": att_b / att_ms / 1e6, "status": tq.device_status()}))
 
 
+def prefill_probe(args):
+    """One layer of the workload's shape: encode a CTX-token prompt's K and V, then run the
+    whole prompt as one causal chunk; per-call times from CUDA events (not a bench line)."""
+    import torch
+    import rotated_bit_kv_tq_gb300 as tq
+    from rotated_bit_kv_tq_gb300 import build
+    build.build()
+    w = workload(args.workload)
+    tt = w.types[0]
+    tq.codebook_init(tt, 0)
+    ctx, Hkv, Hq, D = args.prefill_probe, w.n_kv_heads, w.n_q_heads, w.head_dim
+    k16 = torch.from_numpy(synth.kv_tokens(w, 0, "K", 0, ctx).reshape(ctx, -1)).cuda()
+    v16 = torch.from_numpy(synth.kv_tokens(w, 0, "V", 0, ctx).reshape(ctx, -1)).cuda()
+    kc = tq.KVCache(tt, Hkv, D, capacity_tokens=ctx)
+    vc = tq.KVCache(tt, Hkv, D, capacity_tokens=ctx)
+    tq.encode_kv(kc, vc, k16, v16)
+    q = torch.randn(ctx, Hq, D, generator=torch.Generator().manual_seed(5)).half().cuda()
+    out = torch.empty(ctx, Hq, D, device="cuda")
+    for _ in range(3):
+        tq.attn_prefill(kc, vc, q, out, pos0=0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        tq.attn_prefill(kc, vc, q, out, pos0=0)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / 5
+    print(json.dumps({"probe": w.name, "prompt": ctx, "prefill_us": ms * 1e3,
+                      "tflops": prefill_flops(Hq, D, 0, ctx) / ms / 1e9,
+                      "status": tq.device_status()}))
+
+
 def main():
     args = parse()
     if args.kernel_probe:
         kernel_probe(args)
+        return
+    if args.prefill_probe:
+        prefill_probe(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
