@@ -177,33 +177,51 @@ __global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(con
     const int64_t t_begin = (int64_t)split * p.tokens_per_split;
     const int64_t t_end = min64(len, t_begin + p.tokens_per_split);
     const int n_tiles = t_end > t_begin ? (int)((t_end - t_begin + TT - 1) / TT) : 0;
-    // ---- rotate q once per call: qh = fp16(W q_b * scale * log2(e) / sqrt(128))
-    for (int hb = warp; hb < Hq * NB; hb += kConsumers) {
-        const int h = hb / NB, b = hb - h * NB;
-        const __half *qp = p.q + ((int64_t)seq * Hq + h) * D + b * kBlock + 4 * lane;
-        const uint2 raw = *reinterpret_cast<const uint2 *>(qp);
-        const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-        const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-        float v[4] = {f01.x, f01.y, f23.x, f23.y};
-        apply_signs4(v, p.kc, 4 * lane);   // rotation W D of the K cache
-        warp_fwht4(v, lane);
-        uint2 o;
-        o.x = pack_half2(v[0] * p.score_scale, v[1] * p.score_scale);
-        o.y = pack_half2(v[2] * p.score_scale, v[3] * p.score_scale);
-        // lane = 8 q4 + j holds values 4 lane .. 4 lane + 3 = 32 q4 + 4 j ..
-        *reinterpret_cast<uint2 *>(qh + h * QS + b * kBlock + 16 * (lane & 7) + 4 * (lane >> 3)) = o;
+    // The first tile is requested before the query rotation and the other stages after it:
+    // the rotation's loads then queue behind one tile rather than the whole ring (measured
+    // at 32K context: 23.4 us per call against 25.6 with every stage issued after the
+    // rotation, and 33 with every stage issued before it).
+    auto issue = [&](int i) {
+        const int64_t t0 = t_begin + (int64_t)i * TT;
+        const int nt = (int)min64(TT, t_end - t0);
+        uint8_t *dk = stage0 + (size_t)(i % p.stages) * p.stage_bytes;
+        issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i % p.stages]));
+    };
+    if (tid == 0 && n_tiles > 0) issue(0);
+    // ---- rotate q once per call: qh = fp16(W q_b * scale * log2(e) / sqrt(128)); a warp
+    // loads its (up to four) query blocks at once, then rotates them
+    for (int hb0 = warp; hb0 < Hq * NB; hb0 += 4 * kConsumers) {
+        uint2 qraw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int hb = hb0 + k * kConsumers;
+            const int h = hb / NB, b = hb - h * NB;
+            qraw[k] = hb < Hq * NB
+                          ? *reinterpret_cast<const uint2 *>(p.q + ((int64_t)seq * Hq + h) * D + b * kBlock + 4 * lane)
+                          : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int hb = hb0 + k * kConsumers;
+            if (hb >= Hq * NB) break;
+            const int h = hb / NB, b = hb - h * NB;
+            const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&qraw[k].x));
+            const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&qraw[k].y));
+            float v[4] = {f01.x, f01.y, f23.x, f23.y};
+            apply_signs4(v, p.kc, 4 * lane);   // rotation W D of the K cache
+            warp_fwht4(v, lane);
+            uint2 o;
+            o.x = pack_half2(v[0] * p.score_scale, v[1] * p.score_scale);
+            o.y = pack_half2(v[2] * p.score_scale, v[3] * p.score_scale);
+            // lane = 8 q4 + j holds values 4 lane .. 4 lane + 3 = 32 q4 + 4 j ..
+            *reinterpret_cast<uint2 *>(qh + h * QS + b * kBlock + 16 * (lane & 7) + 4 * (lane >> 3)) = o;
+        }
     }
+    if (tid == 0)
+        for (int i = 1; i < n_tiles && i < p.stages; ++i) issue(i);
     __syncthreads();
 
     bool timed_out = false;
-    // the first `stages` tiles are in flight before any compute starts
-    if (tid == 0)
-        for (int i = 0; i < n_tiles && i < p.stages; ++i) {
-            const int64_t t0 = t_begin + (int64_t)i * TT;
-            const int nt = (int)min64(TT, t_end - t0);
-            uint8_t *dk = stage0 + (size_t)i * p.stage_bytes;
-            issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i]));
-        }
 
     // ================= consumer warps
     const int g = warp % Hkv, sub = warp / Hkv;
