@@ -50,8 +50,9 @@ struct SplitPlan {
 
 SplitPlan plan_splits(int n_seqs, int head_dim, int64_t max_len, int sm_count) {
     SplitPlan pl;
-    // one wave: two CTAs per SM with one 128-value block per head, else one
-    const int64_t ctas = (int64_t)sm_count * (head_dim <= kBlock ? 2 : 1);
+    // one wave of one CTA per SM, whatever the head size
+    (void)head_dim;
+    const int64_t ctas = sm_count;
     const int64_t target = max64(1, (ctas + n_seqs - 1) / n_seqs);
     int64_t tps = (max64(max_len, 1) + target - 1) / target;
     tps = (tps + kTokenAlign - 1) / kTokenAlign * kTokenAlign;

@@ -32,16 +32,17 @@
 namespace tq {
 namespace {
 
-constexpr int kConsumers = 8;              // compute warps (warp 0 lane 0 also issues TMA)
-constexpr int kThreads = 32 * kConsumers;
+// Compute warps per CTA (warp 0 lane 0 also issues the TMA copies), one CTA per SM: 16
+// warps at 128 registers with one 128-value block per head, 8 with two (whose output
+// accumulators need more registers).  Two warps per KV head at 8 KV heads share every
+// tile, so all warps of an SM advance through the same ring and finish together (two
+// CTAs of 8 warps per SM ran unevenly: the later one took 60 % longer).
+__host__ __device__ constexpr int consumers(int nb) { return nb == 1 ? 16 : 8; }
 constexpr int kWarpTokens = 64;            // 4 m-tiles of 16 tokens per warp per tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kWaitLimit = 1u << 26;  // bounded mbarrier wait (tens of ms)
-// CTAs per SM aimed for: two (16 warps, 128 registers each, two stages each) with one
-// 128-value block per head; one with two blocks per head.
-__host__ __device__ constexpr int ctas_per_sm(int nb) { return nb == 1 ? 2 : 1; }
-constexpr size_t kSmemBudget = 220 * 1024;   // per SM
+constexpr size_t kSmemBudget = 220 * 1024;   // per CTA (one per SM)
 
 // Rotated queries in shared memory, in MMA-fragment order: head h, block b, k-step j and
 // lane quarter q4 hold the four values 32 q4 + 4j .. +3 at halfs h*QS + 128 b + 16 j + 4 q4.
@@ -140,7 +141,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 
 template <int TK, int TV, int NB>
-__global__ void __launch_bounds__(kThreads, NB == 1 ? 2 : 1) attn_mma_kernel(const MmaParams p) {
+__global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const MmaParams p) {
+    constexpr int kConsumers = consumers(NB);
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int BK = block_bytes(TK), BV = block_bytes(TV);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -608,7 +610,7 @@ tq_status launch_t(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return TQ_ERR_CUDA;
-    PdlConfig lc(dim3(p.n_splits, n_seqs), dim3(kThreads), smem, stream);
+    PdlConfig lc(dim3(p.n_splits, n_seqs), dim3(32 * consumers(NB)), smem, stream);
     lc.attrs[1].id = cudaLaunchAttributeClusterDimension;
     lc.attrs[1].val.clusterDim.x = kClusterSplits;
     lc.attrs[1].val.clusterDim.y = 1;
@@ -633,15 +635,15 @@ size_t stage_bytes_for(int tile_tokens, size_t rk, size_t rv) {
 
 bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
     const int hkv = k.n_kv_heads, nb = k.head_dim / kBlock, G = n_q_heads / hkv;
-    if (hkv < 1 || hkv > kConsumers || kConsumers % hkv) return false;
     if (nb < 1 || nb > 2 || G > 8) return false;
+    if (hkv < 1 || hkv > consumers(nb) || consumers(nb) % hkv) return false;
     const size_t rk = tq_row_bytes(k.type, hkv, k.head_dim), rv = tq_row_bytes(v.type, hkv, v.head_dim);
     if (rk % 16 || rv % 16) return false;
-    const int TT = kWarpTokens * (kConsumers / hkv);
+    const int TT = kWarpTokens * (consumers(nb) / hkv);
     if (k.page_tokens && k.page_tokens % 16) return false;
     if (v.page_tokens && v.page_tokens % 16) return false;
     const size_t qbytes = q_bytes(n_q_heads, nb);
-    return qbytes + 128 + 2 * stage_bytes_for(TT, rk, rv) <= kSmemBudget / ctas_per_sm(nb);
+    return qbytes + 128 + 2 * stage_bytes_for(TT, rk, rv) <= kSmemBudget;
 }
 
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
@@ -661,7 +663,8 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     p.head_dim = k.head_dim;
     p.n_splits = n_splits;
     p.tokens_per_split = tokens_per_split;
-    p.wph = kConsumers / k.n_kv_heads;
+    const int nb = k.head_dim / kBlock;
+    p.wph = consumers(nb) / k.n_kv_heads;
     p.tile_tokens = kWarpTokens * p.wph;
     p.mul2 = 2u;
     p.mul4 = 4u;
@@ -670,9 +673,8 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     p.hi31 = 1u << 31;
     const size_t stage = stage_bytes_for(p.tile_tokens, p.kc.row_bytes, p.vc.row_bytes);
     p.stage_bytes = (int)stage;
-    const int nb = k.head_dim / kBlock;
     const size_t qbytes = q_bytes(n_q_heads, nb);
-    p.stages = (int)std::min<size_t>(4, (kSmemBudget / ctas_per_sm(nb) - qbytes - 128) / stage);
+    p.stages = (int)std::min<size_t>(4, (kSmemBudget - qbytes - 128) / stage);
     if (p.stages < 2) return TQ_ERR_UNSUPPORTED;
     if (n_splits % kClusterSplits) return TQ_ERR_UNSUPPORTED;
     const size_t cpart = (size_t)n_q_heads * part_stride(k.head_dim) * sizeof(float);

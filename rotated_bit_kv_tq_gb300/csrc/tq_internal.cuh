@@ -171,14 +171,11 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
                           int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
                           float *part, int n_splits, int tokens_per_split, cudaStream_t stream);
 
-// Prompt-chunk attention (tq_prefill.cu).
+// Prompt-chunk attention on the 5th-generation tensor cores (tq_prefill_tc.cu).
 bool prefill_supported(const tq_cache &k, const tq_cache &v, int n_q_heads);
 tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, int32_t seq_id,
                          int64_t pos0, int64_t n_q, int n_q_heads, float scale, float *out,
                          cudaStream_t stream);
-tq_status launch_prefill_tc(const tq_cache &k, const tq_cache &v, const void *q, int32_t seq_id,
-                            int64_t pos0, int64_t n_q, int n_q_heads, float scale, float *out,
-                            cudaStream_t stream);
 
 // Host Lloyd-Max solver (tq_codebook.cpp).
 void solve_codebook(int levels, double *centroids);

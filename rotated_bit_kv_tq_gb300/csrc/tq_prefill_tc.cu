@@ -1,9 +1,15 @@
 // tq_prefill_tc.cu -- causal prompt-chunk attention over the packed cache on the 5th-generation
 // tensor cores (tcgen05: operands in shared memory, accumulators in tensor memory).
 //
-// Same mathematics as tq_prefill.cu ("llama.cpp に TurboQuant を実装": prompt processing over the
-// compressed cache, dequantisation inside the attention tiles; TinyLLaMA article, section 7:
-// the query at position N attends to rows 0..N).  The work split follows the roles the
+// "llama.cpp に TurboQuant を実装": prompt processing runs over the compressed cache as well
+// ("Numbers on real models"), and the roadmap fuses the dequantisation into the Flash-
+// Attention tiles so that K is never materialised in FP16 in HBM ("Current implementation
+// and what's next").  Query token j of the chunk sits at position pos0 + j and attends to
+// rows 0 .. pos0 + j (TinyLLaMA article, section 7, at every position of the chunk).
+// Everything stays in the rotated domain; each output row gets one inverse FWHT at the end.
+//
+// One decoded K/V tile serves every query row of a CTA, so the products are a dense
+// contraction and run on the tensor cores.  The work split follows the roles the
 // tensor-memory model suggests:
 //  - warps 0-7, two threads per row of the 128-row tile (row = TMEM lane, warps q and q + 4
 //    share lanes 32q..32q+31), each thread owning 64 of a tile's 128 keys: rotate the
@@ -657,9 +663,16 @@ tq_status launch_tc_t(const TcParams &p, unsigned n_ctas, cudaStream_t stream) {
 
 }  // namespace
 
-tq_status launch_prefill_tc(const tq_cache &k, const tq_cache &v, const void *q, int32_t seq_id,
-                            int64_t pos0, int64_t n_q, int n_q_heads, float scale, float *out,
-                            cudaStream_t stream) {
+bool prefill_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
+    if (k.head_dim != kBlock || v.head_dim != kBlock) return false;
+    return n_q_heads % k.n_kv_heads == 0 && n_q_heads / k.n_kv_heads <= kTcRows;
+}
+
+tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, int32_t seq_id,
+                         int64_t pos0, int64_t n_q, int n_q_heads, float scale, float *out,
+                         cudaStream_t stream) {
+    if (!prefill_supported(k, v, n_q_heads)) return TQ_ERR_UNSUPPORTED;
+    if (n_q == 0) return TQ_OK;
     TcParams p;
     p.kc = make_view(k);
     p.vc = make_view(v);
