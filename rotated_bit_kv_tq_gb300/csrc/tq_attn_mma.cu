@@ -178,15 +178,22 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     }
     const int64_t t_begin = (int64_t)split * p.tokens_per_split;
     const int64_t t_end = min64(len, t_begin + p.tokens_per_split);
-    const int n_tiles = t_end > t_begin ? (int)((t_end - t_begin + TT - 1) / TT) : 0;
+    // Tile 0 holds TT / 2 tokens, the others TT: with every CTA requesting its first tile
+    // at once, a short first tile arrives sooner and the compute starts while the rest of
+    // the split streams in.
+    const int TF = TT / 2;
+    const int64_t span = t_end - t_begin;
+    const int n_tiles = span <= 0 ? 0 : span <= TF ? 1 : 1 + (int)((span - TF + TT - 1) / TT);
+    auto tile_start = [&](int i) -> int64_t { return t_begin + (i == 0 ? 0 : TF + (int64_t)(i - 1) * TT); };
+    auto tile_len = [&](int i) -> int { return (int)min64(i == 0 ? TF : TT, t_end - tile_start(i)); };
     // Thread 0 requests the first tile as soon as the sequence length is known and the rest
     // of the ring after the rotation; warps 1-7 rotate the query meanwhile, so the query
     // loads and the length load are in flight together (measured at 32K context: 23.2 us
     // per call, against 24.4 with warp 0 rotating too and 25.6 with every stage requested
     // after the rotation).
     auto issue = [&](int i) {
-        const int64_t t0 = t_begin + (int64_t)i * TT;
-        const int nt = (int)min64(TT, t_end - t0);
+        const int64_t t0 = tile_start(i);
+        const int nt = tile_len(i);
         uint8_t *dk = stage0 + (size_t)(i % p.stages) * p.stage_bytes;
         issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i % p.stages]));
     };
@@ -281,7 +288,6 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             ovv[b] = (bv + 34 + 4 * q4) & ~3;
         }
         const Shifts ks = {p.mul2, p.mul4, p.hi16, p.hi30, p.hi31};
-        const int wr0 = sub * kWarpTokens;   // this warp's first row in every tile
 
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % p.stages;
@@ -290,13 +296,14 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                 timed_out = true;
                 break;
             }
-            const int64_t t0 = t_begin + (int64_t)i * TT;
-            const int nt = (int)min64(TT, t_end - t0);
+            const int nt = tile_len(i);
             const uint8_t *Kt = stage0 + (size_t)s * p.stage_bytes;
             const uint8_t *Vt = Kt + (size_t)TT * Rk;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
-            const int hr0 = wr0 + 32 * half;   // first row of these two m-tiles
+            // first row of these two m-tiles: the warps of a KV head take consecutive
+            // 32-row slices of each half of the tile (a first tile is one half)
+            const int hr0 = 32 * (half * p.wph + sub);
             if (hr0 < nt) {
                 // ---------------- scores S^T[token, head] of two m-tiles (32 tokens)
                 float sc[2][4];
@@ -443,10 +450,9 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                 if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)((i / p.stages) & 1))) {
                     record_error(TQ_ERR_DEVICE_TIMEOUT);
                 } else {
-                    const int64_t tn = t_begin + (int64_t)(i + p.stages) * TT;
-                    const int ntn = (int)min64(TT, t_end - tn);
                     uint8_t *dk = stage0 + (size_t)s * p.stage_bytes;
-                    issue_tile(p, seq, tn, ntn, dk, dk + (size_t)TT * Rk, smem_u32(&full[s]));
+                    issue_tile(p, seq, tile_start(i + p.stages), tile_len(i + p.stages), dk,
+                               dk + (size_t)TT * Rk, smem_u32(&full[s]));
                 }
             }
         }
