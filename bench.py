@@ -5,8 +5,9 @@ Workload (default): the Llama-3-8B-shaped KV cache -- 32 layers, 8 KV heads, 32 
 heads, head_dim 128, one sequence, 32,768-token context, turbo3.  One step is the whole
 hot path over one batch of synthetic input:
   1. prefill: tq_encode of the K and V of all 32,768 tokens in all 32 layers;
-  2. 128 decode iterations, each appending one token (tq_encode of K and V, every layer)
-     and running tq_attn_decode over the grown context in every layer.
+  2. 128 decode iterations; in every layer each one calls tq_attn_decode_append, which
+     encodes the new token's K and V into the caches (in the attention launch itself) and
+     attends over the grown context.
 Metric: decode-attention tokens/s (value) and encode GB/s (encode.gbs), with the
 fraction of the measured HBM peak of the dominant kernel (roofline).  Outside the timed
 step, "prefill" times prompt-chunk attention (tq_attn_prefill) on the last 2,048-token
@@ -79,6 +80,13 @@ def attn_bytes(w, ctx, tq_type=3):
     """Algorithmic bytes of one decode-attention launch (one layer, one sequence)."""
     row = w.n_kv_heads * (w.head_dim // 128) * (2 + 128 * tq_type // 8)
     return ctx * 2 * row + w.n_q_heads * w.head_dim * (2 + 4)
+
+
+def append_bytes(w, tq_type=3):
+    """Algorithmic bytes of the decode-step append (one layer, one sequence): the new
+    token's fp16 K and V read, one packed row of each written."""
+    row = w.n_kv_heads * (w.head_dim // 128) * (2 + 128 * tq_type // 8)
+    return 2 * (w.n_kv_heads * w.head_dim * 2 + row)
 
 
 # ------------------------------------------------------------------ clocks
@@ -226,7 +234,6 @@ def run_ours(args, rank, world, local_rank, dist):
     vc = [tq.KVCache(tt, Hkv, D, capacity_tokens=max_len, device=dev) for _ in range(L)]
     out_dev = torch.zeros((L, Hq, D), dtype=torch.float32, device=dev)
     ws = torch.empty(max(16, tq.attn_workspace_bytes(1, Hq, D, max_len)), dtype=torch.uint8, device=dev)
-    pos_dev = torch.zeros(1, dtype=torch.int32, device=dev)
     lens_dev = torch.zeros(1, dtype=torch.int32, device=dev)
     step_dev = torch.zeros(1, dtype=torch.int64, device=dev)
     new_buf = torch.empty((1, L, 2, row), dtype=torch.float16, device=dev)
@@ -235,7 +242,6 @@ def run_ours(args, rank, world, local_rank, dist):
     def prefill():
         for l in range(L):
             tq.encode_kv(kc[l], vc[l], kv_dev[l, 0], kv_dev[l, 1])
-        pos_dev.fill_(T)
         lens_dev.fill_(T + 1)
         step_dev.zero_()
 
@@ -243,9 +249,8 @@ def run_ours(args, rank, world, local_rank, dist):
         torch.index_select(new_dev, 0, step_dev, out=new_buf)
         torch.index_select(q_dev, 0, step_dev, out=q_buf)
         for l in range(L):
-            tq.encode_kv(kc[l], vc[l], new_buf[0, l, 0:1], new_buf[0, l, 1:2], positions=pos_dev)
-            tq.attn_decode(kc[l], vc[l], q_buf[0, l:l + 1], lens_dev, max_len, out_dev[l:l + 1], ws)
-        pos_dev.add_(1)
+            tq.attn_decode_append(kc[l], vc[l], new_buf[0, l, 0:1], new_buf[0, l, 1:2],
+                                  q_buf[0, l:l + 1], lens_dev, max_len, out_dev[l:l + 1], ws)
         lens_dev.add_(1)
         step_dev.add_(1)
 
@@ -292,14 +297,16 @@ def run_ours(args, rank, world, local_rank, dist):
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
     status = tq.device_status()
 
-    # per-launch durations of the attention and encode calls, right after the timed region
+    # per-launch durations of the decode-step and encode calls, right after the timed region
     # and in the same state: each call is replayed from a CUDA graph of the 32 layers' calls
-    # (as in the timed step), bracketed by CUDA events on the replay stream
+    # (as in the timed step), bracketed by CUDA events on the replay stream.  The decode
+    # step re-appends the last iteration's token at the last position (the same bytes).
     lens_dev.fill_(max_len)
     g_att, g_enc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_att, stream=cap, capture_error_mode="thread_local"):
         for l in range(L):
-            tq.attn_decode(kc[l], vc[l], q_buf[0, l:l + 1], lens_dev, max_len, out_dev[l:l + 1], ws)
+            tq.attn_decode_append(kc[l], vc[l], new_buf[0, l, 0:1], new_buf[0, l, 1:2],
+                                  q_buf[0, l:l + 1], lens_dev, max_len, out_dev[l:l + 1], ws)
     with torch.cuda.graph(g_enc, stream=cap, capture_error_mode="thread_local"):
         for l in range(L):
             tq.encode(kc[l], kv_dev[l, 0])
@@ -377,7 +384,7 @@ def run_ours(args, rank, world, local_rank, dist):
     value = job_throughput(world, K * S, dec_ms)
     enc_gbs = world * K * enc_bytes / (pre_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak_hbm()
-    a_bytes = attn_bytes(w, max_len, tt)
+    a_bytes = attn_bytes(w, max_len, tt) + append_bytes(w, tt)
     a_gbs = a_bytes / (attn_launch_ms / 1e3) / 1e9
     e_bytes = encode_bytes_per_token(w, tt) // 2 * T
     e_gbs = e_bytes / (enc_launch_ms / 1e3) / 1e9
@@ -406,7 +413,8 @@ def run_ours(args, rank, world, local_rank, dist):
         "encode": {"gbs": enc_gbs, "tokens_per_s": world * K * T * L / (pre_ms / 1e3),
                    "ms_per_step": pre_ms / K},
         "decode_ms_per_step": dec_ms / K,
-        "roofline": {"kernel": "tq_attn_decode (split-K partial + merge)", "bound": "hbm",
+        "roofline": {"kernel": "tq_attn_decode_append (append + split-K partial + merge)",
+                     "bound": "hbm",
                      "achieved": a_gbs, "peak": peak, "unit": "GB/s", "frac": a_gbs / peak,
                      "peak_source": peak_kind,
                      "traffic": TRAFFIC_PER_TOKEN["attn"] * max_len if TRAFFIC_PER_TOKEN["attn"] else None,
@@ -428,7 +436,7 @@ def run_ours(args, rank, world, local_rank, dist):
                          "frac": pf_tflops / tpeak, "peak_source": tpeak_kind, "traffic": None,
                          "flops_per_launch": prefill_flops(Hq, D, pf_pos0, PREFILL_CHUNK),
                          "launch_ms": pf_ms / L}},
-        "gpu_launches": K * (L + S * L * 3),
+        "gpu_launches": K * (L + S * L * 2),
         "clocks": clk,
         "device_status": status,
         "input_gen_s": t_gen,

@@ -188,6 +188,27 @@ TQ_API tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void
                          int64_t max_seq_len, float softmax_scale, float *out,
                          void *workspace, size_t ws_bytes, void *stream);
 
+/* One decode step of a layer: append each sequence's new token to the caches, then attend
+ * over the positions that include it.  This is the decode-step data flow of the kenji.blog
+ * article, section 8 (the token at position N writes row N, then attends to rows 0..N),
+ * in one call: the result equals tq_encode_kv of the new rows followed by tq_attn_decode.
+ *   k_new_f16,     device fp16 [n_seqs][n_kv_heads][head_dim], 16-byte aligned: the new K
+ *   v_new_f16      and V rows; sequence s's rows are encoded (bit-identical to tq_encode_kv)
+ *                  into position seq_lens[s] - 1 of cache sequence s.  A sequence with
+ *                  seq_lens[s] == 0 appends nothing and gets a zero output.
+ *   other arguments as for tq_attn_decode; seq_lens counts the appended token.
+ * On the tensor-core path the CTA whose split holds position seq_lens[s] - 1 encodes the
+ * rows itself before it reads them, so the step is one attention launch plus the merge;
+ * shapes that path does not take append in a launch of their own first.  A row whose
+ * position the cache cannot address is skipped and TQ_ERR_OUT_OF_RANGE is recorded for
+ * tq_device_status. */
+TQ_API tq_status tq_attn_decode_append(const tq_cache *k, const tq_cache *v,
+                                       const void *k_new_f16, const void *v_new_f16,
+                                       const void *q_f16, int n_seqs, int n_q_heads,
+                                       const int32_t *seq_lens, int64_t max_seq_len,
+                                       float softmax_scale, float *out, void *workspace,
+                                       size_t ws_bytes, void *stream);
+
 /* Causal attention of a prompt chunk (multi-token / prefill) over the packed caches.
  * Query token j of the chunk sits at position pos0 + j and attends to rows 0 .. pos0 + j of
  * cache sequence seq_id: the KV-cache rule of the kenji.blog TinyLLaMA article, section 7

@@ -128,6 +128,18 @@ def attn_decode(k: KVCache, v: KVCache, q, seq_lens, max_seq_len: int, out, work
                                 _ptr(workspace), ws_bytes, _stream_ptr(stream)), "tq_attn_decode")
 
 
+def attn_decode_append(k: KVCache, v: KVCache, k_new, v_new, q, seq_lens, max_seq_len: int, out,
+                       workspace, softmax_scale: float = 0.0, stream=None):
+    """One decode step: k_new / v_new fp16 [n_seqs, n_kv_heads, head_dim] go to position
+    seq_lens[s] - 1 of sequence s, then attention as attn_decode (seq_lens counts them)."""
+    n_seqs, n_q_heads = q.shape[0], q.shape[1]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(load().tq_attn_decode_append(ctypes.byref(k.view), ctypes.byref(v.view), _ptr(k_new),
+                                       _ptr(v_new), _ptr(q), n_seqs, n_q_heads, _ptr(seq_lens),
+                                       max_seq_len, softmax_scale, _ptr(out), _ptr(workspace),
+                                       ws_bytes, _stream_ptr(stream)), "tq_attn_decode_append")
+
+
 def attn_prefill(k: KVCache, v: KVCache, q, out, *, pos0: int, seq_id: int = 0,
                  softmax_scale: float = 0.0, stream=None):
     """Causal attention of a prompt chunk: q fp16 [n_q, n_q_heads, head_dim], query j at

@@ -70,6 +70,11 @@ SIGNATURES = {
                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                       ctypes.c_int64, ctypes.c_float, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "tq_attn_decode_append": (ctypes.c_int, [ctypes.POINTER(TqCache), ctypes.POINTER(TqCache),
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                             ctypes.c_int64, ctypes.c_float, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "tq_attn_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(TqCache), ctypes.POINTER(TqCache),
                                               ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,

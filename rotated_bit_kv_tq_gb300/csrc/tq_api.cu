@@ -196,10 +196,14 @@ size_t tq_attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t 
     return attn_workspace_bytes(n_seqs, n_q_heads, head_dim, max_seq_len, device_sm_count());
 }
 
-tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void *q_f16, int n_seqs,
-                         int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
-                         float softmax_scale, float *out, void *workspace, size_t ws_bytes,
-                         void *stream) {
+}  // extern "C"
+
+namespace {
+// Argument checks shared by tq_attn_decode and tq_attn_decode_append.
+tq_status attn_decode_checked(const tq_cache *k, const tq_cache *v, const void *q_f16, int n_seqs,
+                              int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
+                              float softmax_scale, float *out, void *workspace, size_t ws_bytes,
+                              void *stream, const void *k_new, const void *v_new) {
     tq_status st = validate_cache(k);
     if (st != TQ_OK) return st;
     st = validate_cache(v);
@@ -219,7 +223,31 @@ tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void *q_f16
     if (need > 0 && (!workspace || ws_bytes < need)) return TQ_ERR_WORKSPACE_TOO_SMALL;
     if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16) return TQ_ERR_INVALID_ARGUMENT;
     return launch_attn(*k, *v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len, softmax_scale,
-                       out, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+                       out, workspace, ws_bytes, static_cast<cudaStream_t>(stream), k_new, v_new);
+}
+}  // namespace
+
+extern "C" {
+
+tq_status tq_attn_decode_append(const tq_cache *k, const tq_cache *v, const void *k_new_f16,
+                                const void *v_new_f16, const void *q_f16, int n_seqs,
+                                int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
+                                float softmax_scale, float *out, void *workspace,
+                                size_t ws_bytes, void *stream) {
+    if (!k_new_f16 || reinterpret_cast<uintptr_t>(k_new_f16) % 16 || !v_new_f16 ||
+        reinterpret_cast<uintptr_t>(v_new_f16) % 16)
+        return TQ_ERR_INVALID_ARGUMENT;
+    return attn_decode_checked(k, v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len,
+                               softmax_scale, out, workspace, ws_bytes, stream, k_new_f16,
+                               v_new_f16);
+}
+
+tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void *q_f16, int n_seqs,
+                         int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
+                         float softmax_scale, float *out, void *workspace, size_t ws_bytes,
+                         void *stream) {
+    return attn_decode_checked(k, v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len,
+                               softmax_scale, out, workspace, ws_bytes, stream, nullptr, nullptr);
 }
 
 tq_status tq_attn_prefill(const tq_cache *k, const tq_cache *v, const void *q_f16,

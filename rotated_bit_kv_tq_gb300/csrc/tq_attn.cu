@@ -425,7 +425,8 @@ size_t attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max
 
 tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
                       int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
-                      float *out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+                      float *out, void *ws, size_t ws_bytes, cudaStream_t stream,
+                      const void *k_new, const void *v_new) {
     AttnParams p;
     p.kc = make_view(k);
     p.vc = make_view(v);
@@ -451,13 +452,18 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
         return TQ_ERR_WORKSPACE_TOO_SMALL;
     if (attn_mma_supported(k, v, n_q_heads)) {
         tq_status st = launch_attn_mma(k, v, q, n_seqs, n_q_heads, seq_lens, max_seq_len, scale,
-                                       p.part, p.n_splits, p.tokens_per_split, stream);
+                                       p.part, p.n_splits, p.tokens_per_split, k_new, v_new,
+                                       stream);
         if (st != TQ_OK) return st;
         AttnParams pm = p;
         pm.n_splits = p.n_splits / kClusterSplits;   // one partial row per cluster
         return launch_merge(pm, n_seqs, stream);
     }
     if (p.group > kMaxG || p.nb > kMaxNb) return TQ_ERR_UNSUPPORTED;
+    if (k_new) {   // the fp32 kernel reads the caches only: append in a launch of its own
+        tq_status st = launch_append(k, v, k_new, v_new, seq_lens, n_seqs, stream);
+        if (st != TQ_OK) return st;
+    }
     const int tk = k.type, tv = v.type;
     if (tk == TQ_TURBO3 && tv == TQ_TURBO3) return launch_attn_t<3, 3>(p, n_seqs, stream);
     if (tk == TQ_TURBO2 && tv == TQ_TURBO2) return launch_attn_t<2, 2>(p, n_seqs, stream);

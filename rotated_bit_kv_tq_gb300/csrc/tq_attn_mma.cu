@@ -28,6 +28,7 @@
 #include "tq_internal.cuh"
 #include "tq_simd.cuh"
 #include "tq_codes.cuh"
+#include "tq_encode_warp.cuh"
 
 namespace tq {
 namespace {
@@ -56,6 +57,7 @@ inline size_t q_bytes(int n_q_heads, int nb) {
 struct MmaParams {
     CacheView kc, vc;
     const __half *q;
+    const __half *k_new, *v_new;   // decode-step append: [n_seqs][Hkv][D] fp16, or null
     const int32_t *seq_lens;
     float *part;        // [n_seqs][n_splits][Hq][part_stride(D)]
     float score_scale;  // softmax scale * log2(e) / sqrt(128)
@@ -186,20 +188,37 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     const int n_tiles = span <= 0 ? 0 : span <= TF ? 1 : 1 + (int)((span - TF + TT - 1) / TT);
     auto tile_start = [&](int i) -> int64_t { return t_begin + (i == 0 ? 0 : TF + (int64_t)(i - 1) * TT); };
     auto tile_len = [&](int i) -> int { return (int)min64(i == 0 ? TF : TT, t_end - tile_start(i)); };
+    // ---- decode-step append (k_new set): the CTA whose split holds the new row (position
+    // len - 1, the last row of its last tile) encodes the token's K and V blocks, one warp
+    // per block, after the query rotation, and stores them in the caches.  When that tile's
+    // stage is filled for the first time (the usual case), the blocks are also written
+    // straight into the stage and the tile's TMA copy stops one row short, so the new row
+    // costs no round trip through memory.  Otherwise an async-proxy fence and the barrier
+    // below order the stores before the refill that copies the row; no other CTA reads it.
+    const bool owner = p.k_new && len > 0 && split == (int)((len - 1) / p.tokens_per_split);
+    const int i_new = owner ? n_tiles - 1 : -1;            // the tile holding the new row
+    const bool new_in_stage = owner && i_new < p.stages;
+    const int bpr = Hkv * NB;
+    auto enc_src = [&](int bi) -> const __half * {
+        const int c = bi >= bpr ? 1 : 0;
+        return (c ? p.v_new : p.k_new) + ((int64_t)seq * bpr + (bi - c * bpr)) * kBlock;
+    };
+    uint2 enc_raw = make_uint2(0u, 0u);   // this warp's first block, loaded with the query
+    if (owner && warp < 2 * bpr) enc_raw = warp_block_load(enc_src(warp), lane);
     // Thread 0 requests the first tile as soon as the sequence length is known and the rest
-    // of the ring after the rotation; warps 1-7 rotate the query meanwhile, so the query
+    // of the ring after the rotation; warps 1-15 rotate the query meanwhile, so the query
     // loads and the length load are in flight together (measured at 32K context: 23.2 us
     // per call, against 24.4 with warp 0 rotating too and 25.6 with every stage requested
     // after the rotation).
     auto issue = [&](int i) {
         const int64_t t0 = tile_start(i);
-        const int nt = tile_len(i);
+        const int nt = tile_len(i) - (i == i_new && new_in_stage ? 1 : 0);
         uint8_t *dk = stage0 + (size_t)(i % p.stages) * p.stage_bytes;
         issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i % p.stages]));
     };
     if (tid == 0 && n_tiles > 0) issue(0);
     // ---- rotate q once per call: qh = fp16(W q_b * scale * log2(e) / sqrt(128)) by warps
-    // 1-7; a warp loads its (up to five) query blocks at once, then rotates them
+    // 1-15; a warp loads its (up to five) query blocks at once, then rotates them
     constexpr int kRot = kConsumers - 1;
     if (warp > 0)
     for (int hb0 = warp - 1; hb0 < Hq * NB; hb0 += 5 * kRot) {
@@ -229,8 +248,31 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             *reinterpret_cast<uint2 *>(qh + h * QS + b * kBlock + 16 * (lane & 7) + 4 * (lane >> 3)) = o;
         }
     }
-    if (tid == 0)
+    if (tid == 0)   // no copy in this loop reads the new row (see above)
         for (int i = 1; i < n_tiles && i < p.stages; ++i) issue(i);
+    if (owner) {
+        // the new row's slot in its stage (used when new_in_stage)
+        uint8_t *sk = stage0 + (size_t)(i_new % p.stages) * p.stage_bytes;
+        const int r_new = tile_len(i_new) - 1;
+        for (int bi = warp; bi < 2 * bpr; bi += kConsumers) {
+            const int c = bi >= bpr ? 1 : 0, jb = bi - c * bpr;
+            const CacheView &cv = c ? p.vc : p.kc;
+            const uint2 raw = bi == warp ? enc_raw : warp_block_load(enc_src(bi), lane);
+            uint8_t *row = nullptr;
+            if (lane == 0) row = row_ptr(cv, seq, len - 1);   // records an out-of-range row once
+            row = reinterpret_cast<uint8_t *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(row), 0));
+            if (c) {
+                const WarpBlock wb = warp_encode_raw<TV>(raw, cv, lane);
+                if (row) warp_store_block<TV>(row + jb * BV, wb, lane);
+                if (new_in_stage) warp_store_block<TV>(sk + (size_t)TT * Rk + (size_t)r_new * Rv + jb * BV, wb, lane);
+            } else {
+                const WarpBlock wb = warp_encode_raw<TK>(raw, cv, lane);
+                if (row) warp_store_block<TK>(row + jb * BK, wb, lane);
+                if (new_in_stage) warp_store_block<TK>(sk + (size_t)r_new * Rk + jb * BK, wb, lane);
+            }
+        }
+        if (!new_in_stage) asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    }
     __syncthreads();
 
     bool timed_out = false;
@@ -654,11 +696,14 @@ bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
 
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
                           int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
-                          float *part, int n_splits, int tokens_per_split, cudaStream_t stream) {
+                          float *part, int n_splits, int tokens_per_split, const void *k_new,
+                          const void *v_new, cudaStream_t stream) {
     MmaParams p;
     p.kc = make_view(k);
     p.vc = make_view(v);
     p.q = static_cast<const __half *>(q);
+    p.k_new = static_cast<const __half *>(k_new);
+    p.v_new = static_cast<const __half *>(v_new);
     p.seq_lens = seq_lens;
     p.part = part;
     p.score_scale = scale * kLog2e * kInvSqrt128;

@@ -20,6 +20,7 @@
 // f32x2 instructions and __f*_rn intrinsics are never fused).
 #include "tq_internal.cuh"
 #include "tq_simd.cuh"
+#include "tq_encode_warp.cuh"
 
 namespace tq {
 namespace {
@@ -33,6 +34,7 @@ struct EncodeParams {
     int64_t stride;            // elements between token rows of src
     const int32_t *seq_ids;    // or nullptr
     const int32_t *positions;  // or nullptr
+    const int32_t *lens;       // decode-step append: token t -> sequence t, position lens[t] - 1
     int64_t pos0;
     int64_t n_tokens;
     int64_t n_tiles;
@@ -72,18 +74,6 @@ __device__ __forceinline__ void load_tile(const EncodeParams &p, int64_t tile, u
 // exponent bit) is 0 and each value lands as (sign, 0) at bits (2j+1, 2j).
 __device__ __forceinline__ uint32_t collect2(uint32_t w, float v) {
     return __funnelshift_l(__float_as_uint(v), w, 2);
-}
-
-// Squared centroid of a value's code: it depends only on the magnitude index
-// m = #{positive thresholds below |y|} (the codebook is symmetric).
-template <int TYPE>
-__device__ __forceinline__ float code_sq(const Codebook &cb, float y) {
-    constexpr int L = 1 << TYPE;
-    const float a = fabsf(y);
-    int m = a > cb.threshold[L / 2] ? 1 : 0;
-    if (TYPE == TQ_TURBO3) m += (a > cb.threshold[5] ? 1 : 0) + (a > cb.threshold[6] ? 1 : 0);
-    const float c = cb.centroid[L / 2 + m];
-    return __fmul_rn(c, c);
 }
 
 template <int TYPE>
@@ -323,11 +313,8 @@ tq_status launch_encode_t(const EncodeParams &p0, const EncodeParams &p1, int n_
 // ------------------------------------------------------------------ small appends
 // A decode step appends one token (or one per sequence): a few hundred blocks at most,
 // too few to fill the GPU with one block per thread.  Here a warp encodes one block, four
-// values per lane, so the latency of a block is that of ~200 instructions.  The operation
-// order is the one of encode_one: the norm tree pairs element i with i + len/2 (lanes
-// xor 16, 8, 4, 2, 1, then in-lane), butterflies run h = 1, 2 (in-lane) and 4 .. 64
-// (lanes xor 1 .. 16), every operation rounded separately, so the codes and norms are
-// the same bits.
+// values per lane (tq_encode_warp.cuh, in the operation order of encode_one, so the codes
+// and norms are the same bits), and the latency of a block is that of ~200 instructions.
 constexpr int kWarpPathWarps = 8;               // warps (blocks) per CTA
 constexpr int64_t kWarpPathMaxBlocks = 4096;    // larger calls use encode_kernel
 
@@ -337,106 +324,21 @@ __global__ void __launch_bounds__(32 * kWarpPathWarps) encode_warp_kernel(const 
     pdl_wait();
     pdl_launch_dependents();
     const EncodeParams &p = blockIdx.y ? p1 : p0;
-    const Codebook &cb = c_codebook[cb_index(TYPE)];
-    constexpr int L = 1 << TYPE, B = block_bytes(TYPE);
+    constexpr int B = block_bytes(TYPE);
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kWarpPathWarps + (threadIdx.x >> 5);
     if (gw >= p.n_tokens * p.bpr) return;   // whole warp
     const int64_t t = gw / p.bpr;
     const int jb = (int)(gw - t * p.bpr);
-    // values 4 lane .. 4 lane + 3 of the block
-    const uint2 raw = *reinterpret_cast<const uint2 *>(p.src + t * p.stride + jb * kBlock + 4 * lane);
-    const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-    const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-    float x[4] = {f01.x, f01.y, f23.x, f23.y};
-    if (p.dst.has_signs) {   // rotation-sign variant: W D
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = __uint_as_float(__float_as_uint(x[e]) ^ sign_mask(p.dst, 4 * lane + e));
-    }
-    // norm
-    float sq[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sq[e] = __fmul_rn(x[e], x[e]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sq[e] = __fadd_rn(sq[e], __shfl_xor_sync(0xffffffffu, sq[e], off));
-    const float n = __fsqrt_rn(__fadd_rn(__fadd_rn(sq[0], sq[2]), __fadd_rn(sq[1], sq[3])));
-    uint16_t norm16 = __half_as_ushort(__float2half_rn(fminf(n, 65504.0f)));
-    const float k = n > 0.0f ? __fdiv_rn(kInvSqrt128, n) : 0.0f;
-    // butterflies
-    {
-        const float a0 = __fadd_rn(x[0], x[1]), a1 = __fsub_rn(x[0], x[1]);
-        const float a2 = __fadd_rn(x[2], x[3]), a3 = __fsub_rn(x[2], x[3]);
-        x[0] = __fadd_rn(a0, a2);
-        x[2] = __fsub_rn(a0, a2);
-        x[1] = __fadd_rn(a1, a3);
-        x[3] = __fsub_rn(a1, a3);
-    }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = lane & m;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
-            x[e] = upper ? __fsub_rn(o, x[e]) : __fadd_rn(x[e], o);
-        }
-    }
-    // sign-magnitude quantiser: m = #{positive thresholds strictly below |y|},
-    // code = signbit(y) ? L/2 - 1 - m : L/2 + m; pack into this lane's share of the words
-    float ys[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) ys[e] = __fmul_rn(x[e], k);
-    if (p.dst.norm_correction) {   // store |x| / |c|, |c| over the norm's pairwise tree
-        float c2[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) c2[e] = code_sq<TYPE>(cb, ys[e]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) c2[e] = __fadd_rn(c2[e], __shfl_xor_sync(0xffffffffu, c2[e], off));
-        const float cn = __fsqrt_rn(__fadd_rn(__fadd_rn(c2[0], c2[2]), __fadd_rn(c2[1], c2[3])));
-        norm16 = __half_as_ushort(__float2half_rn(fminf(__fdiv_rn(n, cn), 65504.0f)));
-    }
-    uint32_t wlo = 0, whi = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float y = ys[e];
-        const float a = fabsf(y);
-        uint32_t m = 0;
-#pragma unroll
-        for (int j = L / 2; j <= L - 2; ++j) m += a > cb.threshold[j] ? 1u : 0u;
-        const uint32_t c = signbit(y) ? (uint32_t)(L / 2 - 1) - m : (uint32_t)(L / 2) + m;
-        const int jl = 4 * (lane & 3) + e;          // value index within its 16-value word
-        wlo |= (c & 3u) << (4 * (jl & 7) + 2 * (jl >> 3));
-        if (TYPE == TQ_TURBO3) {
-            const int jh = 4 * (lane & 7) + e;      // value index within its 32-value word
-            whi |= (c >> 2) << (4 * (jh & 7) + (jh >> 3));
-        }
-    }
-    wlo |= __shfl_xor_sync(0xffffffffu, wlo, 1);
-    wlo |= __shfl_xor_sync(0xffffffffu, wlo, 2);
-    if (TYPE == TQ_TURBO3) {
-        whi |= __shfl_xor_sync(0xffffffffu, whi, 1);
-        whi |= __shfl_xor_sync(0xffffffffu, whi, 2);
-        whi |= __shfl_xor_sync(0xffffffffu, whi, 4);
-    }
-    const int64_t seq = p.seq_ids ? (int64_t)p.seq_ids[t] : (int64_t)p.seq_id;
-    const int64_t pos = p.positions ? (int64_t)p.positions[t] : p.pos0 + t;
+    const WarpBlock wb = warp_encode_block<TYPE>(p.src + t * p.stride + jb * kBlock, p.dst, lane);
+    const int64_t seq = p.seq_ids ? (int64_t)p.seq_ids[t] : p.lens ? t : (int64_t)p.seq_id;
+    const int64_t pos = p.lens ? (int64_t)p.lens[t] - 1 : p.positions ? (int64_t)p.positions[t] : p.pos0 + t;
+    if (p.lens && pos < 0) return;   // an empty sequence appends nothing
     uint8_t *row = nullptr;
     if (lane == 0) row = row_ptr(p.dst, seq, pos);   // records an out-of-range row once
     row = reinterpret_cast<uint8_t *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(row), 0));
     if (!row) return;
-    uint16_t *o = reinterpret_cast<uint16_t *>(row + (int64_t)jb * B);   // 2-byte aligned
-    if (lane == 0) o[0] = norm16;
-    if ((lane & 3) == 0) {
-        o[1 + 2 * (lane >> 2)] = (uint16_t)(wlo & 0xffffu);
-        o[2 + 2 * (lane >> 2)] = (uint16_t)(wlo >> 16);
-    }
-    if (TYPE == TQ_TURBO3 && (lane & 7) == 0) {
-        o[17 + 2 * (lane >> 3)] = (uint16_t)(whi & 0xffffu);
-        o[18 + 2 * (lane >> 3)] = (uint16_t)(whi >> 16);
-    }
+    warp_store_block<TYPE>(row + (int64_t)jb * B, wb, lane);
 }
 
 template <int TYPE>
@@ -466,6 +368,7 @@ EncodeParams make_params(const tq_cache &dst, const void *src, int64_t n_tokens,
     p.stride = stride;
     p.seq_ids = seq_ids;
     p.positions = positions;
+    p.lens = nullptr;
     p.pos0 = pos0;
     p.n_tokens = n_tokens;
     p.seq_id = seq_id;
@@ -503,6 +406,27 @@ tq_status launch_encode_kv(const tq_cache &k, const tq_cache &v, const void *k_s
     }
     return k.type == TQ_TURBO3 ? launch_encode_any<TQ_TURBO3>(pk, pv, 2, stream)
                                : launch_encode_any<TQ_TURBO2>(pk, pv, 2, stream);
+}
+
+// Decode-step append for shapes the fused attention kernel does not take: sequence s's new
+// K and V rows ([n_seqs][Hkv][D] fp16) go to position seq_lens[s] - 1 (none if 0).
+tq_status launch_append(const tq_cache &k, const tq_cache &v, const void *k_new, const void *v_new,
+                        const int32_t *seq_lens, int n_seqs, cudaStream_t stream) {
+    EncodeParams pk = make_params(k, k_new, n_seqs, (int64_t)k.n_kv_heads * k.head_dim, nullptr,
+                                  nullptr, 0, 0);
+    EncodeParams pv = make_params(v, v_new, n_seqs, (int64_t)v.n_kv_heads * v.head_dim, nullptr,
+                                  nullptr, 0, 0);
+    pk.lens = seq_lens;
+    pv.lens = seq_lens;
+    if (k.type != v.type) {
+        tq_status st = k.type == TQ_TURBO3 ? launch_encode_warp_t<TQ_TURBO3>(pk, pk, 1, stream)
+                                           : launch_encode_warp_t<TQ_TURBO2>(pk, pk, 1, stream);
+        if (st != TQ_OK) return st;
+        return v.type == TQ_TURBO3 ? launch_encode_warp_t<TQ_TURBO3>(pv, pv, 1, stream)
+                                   : launch_encode_warp_t<TQ_TURBO2>(pv, pv, 1, stream);
+    }
+    return k.type == TQ_TURBO3 ? launch_encode_warp_t<TQ_TURBO3>(pk, pv, 2, stream)
+                               : launch_encode_warp_t<TQ_TURBO2>(pk, pv, 2, stream);
 }
 
 }  // namespace tq

@@ -161,15 +161,21 @@ tq_status launch_decode(const tq_cache &src, int32_t seq_id, int64_t pos0, int64
                         float *dst, cudaStream_t stream);
 size_t attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max_seq_len,
                             int sm_count);
+// k_new / v_new (fp16 [n_seqs][Hkv][D], or null): append sequence s's new token at position
+// seq_lens[s] - 1 before attending (the tensor-core kernel does it in the same launch).
 tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
                       int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
-                      float *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+                      float *out, void *ws, size_t ws_bytes, cudaStream_t stream,
+                      const void *k_new = nullptr, const void *v_new = nullptr);
+tq_status launch_append(const tq_cache &k, const tq_cache &v, const void *k_new, const void *v_new,
+                        const int32_t *seq_lens, int n_seqs, cudaStream_t stream);
 
 // Tensor-core decode attention (tq_attn_mma.cu): writes split partials like the fp32 kernel.
 bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads);
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
                           int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
-                          float *part, int n_splits, int tokens_per_split, cudaStream_t stream);
+                          float *part, int n_splits, int tokens_per_split, const void *k_new,
+                          const void *v_new, cudaStream_t stream);
 
 // Prompt-chunk attention on the 5th-generation tensor cores (tq_prefill_tc.cu).
 bool prefill_supported(const tq_cache &k, const tq_cache &v, int n_q_heads);
