@@ -198,10 +198,9 @@ TQ_API tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void
  *                  seq_lens[s] == 0 appends nothing and gets a zero output.
  *   other arguments as for tq_attn_decode; seq_lens counts the appended token.
  * On the tensor-core path the CTA whose split holds position seq_lens[s] - 1 encodes the
- * rows itself before it reads them, so the step is one attention launch plus the merge;
- * shapes that path does not take append in a launch of their own first.  A row whose
- * position the cache cannot address is skipped and TQ_ERR_OUT_OF_RANGE is recorded for
- * tq_device_status. */
+ * rows itself, so the step is one attention launch plus the merge; shapes that path does
+ * not take append in a launch of their own first.  A row whose position the cache cannot
+ * address is skipped and TQ_ERR_OUT_OF_RANGE is recorded for tq_device_status. */
 TQ_API tq_status tq_attn_decode_append(const tq_cache *k, const tq_cache *v,
                                        const void *k_new_f16, const void *v_new_f16,
                                        const void *q_f16, int n_seqs, int n_q_heads,

@@ -142,7 +142,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
-template <int TK, int TV, int NB>
+// APPEND: the decode-step form (p.k_new set); a separate instantiation, so that the plain
+// attention carries none of its code.
+template <int TK, int TV, int NB, bool APPEND>
 __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const MmaParams p) {
     constexpr int kConsumers = consumers(NB);
     extern __shared__ __align__(128) uint8_t smem[];
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     // straight into the stage and the tile's TMA copy stops one row short, so the new row
     // costs no round trip through memory.  Otherwise an async-proxy fence and the barrier
     // below order the stores before the refill that copies the row; no other CTA reads it.
-    const bool owner = p.k_new && len > 0 && split == (int)((len - 1) / p.tokens_per_split);
+    const bool owner = APPEND && len > 0 && split == (int)((len - 1) / p.tokens_per_split);
     const int i_new = owner ? n_tiles - 1 : -1;            // the tile holding the new row
     const bool new_in_stage = owner && i_new < p.stages;
     const int bpr = Hkv * NB;
@@ -261,7 +263,13 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             uint8_t *row = nullptr;
             if (lane == 0) row = row_ptr(cv, seq, len - 1);   // records an out-of-range row once
             row = reinterpret_cast<uint8_t *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(row), 0));
-            if (c) {
+            if (TK == TV) {   // one call site: the second copy of the encoder slowed the main loop
+                const WarpBlock wb = warp_encode_raw<TK>(raw, cv, lane);
+                uint8_t *srow = c ? sk + (size_t)TT * Rk + (size_t)r_new * Rv : sk + (size_t)r_new * Rk;
+                const int bb = c ? BV : BK;
+                if (row) warp_store_block<TK>(row + jb * bb, wb, lane);
+                if (new_in_stage) warp_store_block<TK>(srow + jb * bb, wb, lane);
+            } else if (c) {
                 const WarpBlock wb = warp_encode_raw<TV>(raw, cv, lane);
                 if (row) warp_store_block<TV>(row + jb * BV, wb, lane);
                 if (new_in_stage) warp_store_block<TV>(sk + (size_t)TT * Rk + (size_t)r_new * Rv + jb * BV, wb, lane);
@@ -651,11 +659,11 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-template <int TK, int TV, int NB>
-tq_status launch_t(const MmaParams &p, int n_seqs, cudaStream_t stream) {
+template <int TK, int TV, int NB, bool APPEND>
+tq_status launch_tt(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     const size_t qbytes = q_bytes(p.n_q_heads, NB);
     const size_t smem = qbytes + 128 + (size_t)p.stages * p.stage_bytes;
-    if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB>,
+    if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB, APPEND>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return TQ_ERR_CUDA;
     PdlConfig lc(dim3(p.n_splits, n_seqs), dim3(32 * consumers(NB)), smem, stream);
@@ -664,7 +672,13 @@ tq_status launch_t(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     lc.attrs[1].val.clusterDim.y = 1;
     lc.attrs[1].val.clusterDim.z = 1;
     lc.cfg.numAttrs = 2;
-    return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_mma_kernel<TK, TV, NB>, p));
+    return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_mma_kernel<TK, TV, NB, APPEND>, p));
+}
+
+template <int TK, int TV, int NB>
+tq_status launch_t(const MmaParams &p, int n_seqs, cudaStream_t stream) {
+    return p.k_new ? launch_tt<TK, TV, NB, true>(p, n_seqs, stream)
+                   : launch_tt<TK, TV, NB, false>(p, n_seqs, stream);
 }
 
 template <int NB>
