@@ -40,6 +40,7 @@ struct EncodeParams {
     int64_t n_tiles;
     int32_t seq_id;
     int32_t bpr;               // blocks per token row
+    int32_t src_dense;         // stride == bpr * 128: the source rows form one byte run
     uint32_t bpr_magic;        // div_magic(bpr)
     int32_t rows_per_tile;
     int32_t row_bytes;
@@ -58,8 +59,21 @@ struct EncodeSmem {
 __device__ __forceinline__ void load_tile(const EncodeParams &p, int64_t tile, uint8_t *buf) {
     const int64_t row0 = tile * p.rows_per_tile;
     const int rows = (int)min64(p.rows_per_tile, p.n_tokens - row0);
-    const int chunks = rows * p.bpr * 16;
     const uint32_t sbase = smem_u32(buf);
+    if (p.src_dense) {
+        // Token rows back to back: the tile is one byte run and chunk c = threadIdx.x + 128 i
+        // of it belongs to block f = threadIdx.x / 16 + 8 i at the same 16-byte slot
+        // j = threadIdx.x % 16, with the same swizzle f % 8, so every copy is a fixed offset.
+        const int f0 = threadIdx.x >> 4, j = threadIdx.x & 15;
+        const int nblk = rows * p.bpr;
+        const uint8_t *g = reinterpret_cast<const uint8_t *>(p.src + row0 * p.stride) + threadIdx.x * 16;
+        const uint32_t s = sbase + f0 * 256 + ((j ^ (f0 & 7)) << 4);
+#pragma unroll
+        for (int i = 0; i < kThreads / 8; ++i)
+            if (f0 + 8 * i < nblk) cp_async16(s + i * 2048, g + i * 2048);
+        return;
+    }
+    const int chunks = rows * p.bpr * 16;
     for (int c = threadIdx.x; c < chunks; c += kThreads) {
         const int f = c >> 4, j = c & 15;
         const int r = (int)fast_div((uint32_t)f, p.bpr_magic);
@@ -143,37 +157,54 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
             x[i + h + 1] = d.y;
         }
     }
-    // ---- 4. scale to the unit sphere (|y| <= 1 up to rounding)
+    // ---- 4-5. scale to the unit sphere and take the sign-magnitude Lloyd-Max index,
+    // bit-parallel.  y = fl(z k) with k >= +0, so sign(y) is the sign of z and
+    // |y| = fl(|z| k) (rounding to nearest is symmetric): the magnitudes are scaled in
+    // pairs and the thresholds subtracted in pairs.  "|y| > t" is the sign bit of
+    // fl(t - |y|) (exact zero only when |y| == t, which is not "greater").  Low-plane word
+    // w holds value i = 16w + 8r + k at bits 4k+2r (code bit 0) and 4k+2r+1 (code bit 1):
+    // collecting values in the order j = 2k + r, last first, puts value j's predicate at
+    // bit 2j+1.
     const float2 kk = make_float2(k, k);
-#pragma unroll
-    for (int i = 0; i < kBlock; i += 2) {
-        const float2 y2 = mul2(make_float2(x[i], x[i + 1]), kk);
-        x[i] = y2.x;
-        x[i + 1] = y2.y;
-    }
-    // ---- 5. sign-magnitude Lloyd-Max index, bit-parallel.
-    // "|y| > t" is the sign bit of fl(t - |y|) (exact zero only when |y| == t, which is
-    // not "greater"); sign(y) is the sign bit of y.  Low-plane word w holds value
-    // i = 16w + 8r + k at bits 4k+2r (code bit 0) and 4k+2r+1 (code bit 1): collecting
-    // values in the order j = 2k + r, last first, puts value j's predicate at bit 2j+1.
     uint32_t W[8], SP[8];
     const float t_lo = TYPE == TQ_TURBO3 ? cb.threshold[4] : cb.threshold[2];
     const float t_mid = TYPE == TQ_TURBO3 ? cb.threshold[5] : 0.0f;
     const float t_hi = TYPE == TQ_TURBO3 ? cb.threshold[6] : 0.0f;
+    const float2 t_lo2 = make_float2(t_lo, t_lo), t_mid2 = make_float2(t_mid, t_mid),
+                 t_hi2 = make_float2(t_hi, t_hi);
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
+        float d4[16], d5[16], d6[16];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int kp = 0; kp < 8; kp += 2) {
+                const int i = 16 * w + 8 * r + kp;
+                const float2 u = mul2(make_float2(fabsf(x[i]), fabsf(x[i + 1])), kk);
+                const float2 a = sub2(t_lo2, u);
+                d4[2 * kp + r] = a.x;
+                d4[2 * kp + 2 + r] = a.y;
+                if (TYPE == TQ_TURBO3) {
+                    const float2 b = sub2(t_mid2, u), c = sub2(t_hi2, u);
+                    d5[2 * kp + r] = b.x;
+                    d5[2 * kp + 2 + r] = b.y;
+                    d6[2 * kp + r] = c.x;
+                    d6[2 * kp + 2 + r] = c.y;
+                }
+            }
+        }
         uint32_t ps = 0, p4 = 0, p5 = 0, p6 = 0;
 #pragma unroll
         for (int j = 15; j >= 0; --j) {
-            const float y = x[16 * w + 8 * (j & 1) + (j >> 1)];
-            const float a = fabsf(y);
-            ps = collect2(ps, y);
-            p4 = collect2(p4, __fsub_rn(t_lo, a));
+            ps = collect2(ps, x[16 * w + 8 * (j & 1) + (j >> 1)]);
+            p4 = collect2(p4, d4[j]);
             if (TYPE == TQ_TURBO3) {
-                p5 = collect2(p5, __fsub_rn(t_mid, a));
-                p6 = collect2(p6, __fsub_rn(t_hi, a));
+                p5 = collect2(p5, d5[j]);
+                p6 = collect2(p6, d6[j]);
             }
         }
+        // z may reach |z| >= 2, whose top exponent bit lands at the even positions
+        ps &= 0xAAAAAAAAu;
         if (TYPE == TQ_TURBO3) {
             // m = (|y|>t4) + (|y|>t5) + (|y|>t6): bit1 = |y|>t5, bit0 = |y|>(bit1 ? t6 : t4);
             // code & 3 = m ^ 3s  -> fields (bit1 ^ s, bit0 ^ s)
@@ -198,12 +229,14 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
         }
     }
     // norm-correction variant: store |x| / |c|, |c| over the same pairwise tree as the norm
+    // (x still holds z here; y = fl(z k) as above)
     uint16_t norm_out = norm16;
     if (cv.norm_correction) {
         float c2[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i)
-            c2[i] = __fadd_rn(code_sq<TYPE>(cb, x[i]), code_sq<TYPE>(cb, x[i + 64]));
+            c2[i] = __fadd_rn(code_sq<TYPE>(cb, __fmul_rn(x[i], k)),
+                              code_sq<TYPE>(cb, __fmul_rn(x[i + 64], k)));
 #pragma unroll
         for (int len = 64; len > 1; len >>= 1)
 #pragma unroll
@@ -249,14 +282,26 @@ __global__ void __launch_bounds__(kThreads, 3) encode_kernel(const EncodeParams 
 
         const int64_t row0 = tile * p.rows_per_tile;
         const int rows = (int)min64(p.rows_per_tile, p.n_tokens - row0);
+        // The tile's destination rows form one byte run when every row is valid and lies R
+        // bytes after the one before; each row thread checks its row against the first.
+        bool in_run = true;
         if (threadIdx.x < rows) {
             const int64_t t = row0 + threadIdx.x;
             const int64_t seq = p.seq_ids ? (int64_t)p.seq_ids[t] : (int64_t)p.seq_id;
             const int64_t pos = p.positions ? (int64_t)p.positions[t] : p.pos0 + t;
-            sm.rowdst[threadIdx.x] = row_ptr(p.dst, seq, pos);
+            uint8_t *d = row_ptr(p.dst, seq, pos);
+            sm.rowdst[threadIdx.x] = d;
+            if (threadIdx.x > 0) {
+                const int64_t seq0 = p.seq_ids ? (int64_t)p.seq_ids[row0] : (int64_t)p.seq_id;
+                const int64_t pos0 = p.positions ? (int64_t)p.positions[row0] : p.pos0 + row0;
+                const uint8_t *d0 = row_ptr(p.dst, seq0, pos0);
+                in_run = d0 && d == d0 + (int64_t)threadIdx.x * p.row_bytes;
+            } else {
+                in_run = d != nullptr;
+            }
         }
         cp_async_wait<1>();
-        __syncthreads();
+        const bool run = __syncthreads_and(in_run) && (p.row_bytes & 15) == 0;
 
         const int nblk = rows * p.bpr;
         const int f = threadIdx.x;
@@ -265,7 +310,11 @@ __global__ void __launch_bounds__(kThreads, 3) encode_kernel(const EncodeParams 
 
         // ---- write whole rows out
         const int R = p.row_bytes;
-        if ((R & 15) == 0) {
+        if (run) {
+            uint4 *d = reinterpret_cast<uint4 *>(sm.rowdst[0]);
+            const uint4 *o = reinterpret_cast<const uint4 *>(sm.out);
+            for (int c = threadIdx.x; c < rows * (R >> 4); c += kThreads) d[c] = o[c];
+        } else if ((R & 15) == 0) {
             const int cpr = R >> 4;
             for (int c = threadIdx.x; c < rows * cpr; c += kThreads) {
                 const int r = (int)fast_div((uint32_t)c, p.cpr_magic);
@@ -374,6 +423,7 @@ EncodeParams make_params(const tq_cache &dst, const void *src, int64_t n_tokens,
     p.seq_id = seq_id;
     p.bpr = dst.n_kv_heads * (dst.head_dim / kBlock);
     p.bpr_magic = div_magic((uint32_t)p.bpr);
+    p.src_dense = stride == (int64_t)p.bpr * kBlock;
     p.rows_per_tile = kThreads / p.bpr;
     p.n_tiles = (n_tokens + p.rows_per_tile - 1) / p.rows_per_tile;
     p.row_bytes = p.dst.row_bytes;
