@@ -16,8 +16,9 @@
 //
 // Bit-exactness with the oracle: the same fixed operation order (pairwise norm tree
 // i + len/2, butterfly stages h = 1..64, one IEEE sqrt and one IEEE divide, one multiply
-// per value), every operation rounded separately (no FMA contraction anywhere: the
-// f32x2 instructions and __f*_rn intrinsics are never fused).
+// per value), every operation rounded separately (no FMA contraction: the f32x2
+// instructions and __f*_rn intrinsics are never fused; the one explicit fused multiply-add,
+// on the first level of the norm tree, squares an fp16 value, whose square is exact).
 #include "tq_internal.cuh"
 #include "tq_simd.cuh"
 #include "tq_encode_warp.cuh"
@@ -113,12 +114,13 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
         for (int i = 0; i < kBlock; ++i) x[i] = __uint_as_float(__float_as_uint(x[i]) ^ sign_mask(cv, i));
     }
     // ---- 2. norm: pairwise tree, element i pairs with i + len/2 at every level
+    // (x comes from fp16: 11 significant bits, so x*x is exact in binary32 and the fused
+    // x_i * x_i + fl(x_{i+64}^2) rounds once, like fl(fl(x_i^2) + fl(x_{i+64}^2)))
     float s1[64];
 #pragma unroll
     for (int i = 0; i < 64; i += 2) {
-        const float2 a = mul2(make_float2(x[i], x[i + 1]), make_float2(x[i], x[i + 1]));
         const float2 b = mul2(make_float2(x[i + 64], x[i + 65]), make_float2(x[i + 64], x[i + 65]));
-        const float2 r = add2(a, b);
+        const float2 r = fma2(make_float2(x[i], x[i + 1]), make_float2(x[i], x[i + 1]), b);
         s1[i] = r.x;
         s1[i + 1] = r.y;
     }

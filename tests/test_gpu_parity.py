@@ -130,6 +130,57 @@ def test_encode_paged_scattered(tq):
         assert np.array_equal(pool[row], ref[i])
 
 
+LARGE_ENCODE_CASES = [
+    # (type, n_kv_heads, head_dim, tokens, extra source stride, pos0): more than 4,096
+    # blocks, so the one-thread-per-block encoder runs
+    (3, 8, 128, 1100, 0, 0),      # dense source, one byte run per tile
+    (2, 2, 256, 1500, 24, 37),    # strided source, offset rows, 2-byte stores
+    (3, 5, 256, 500, 0, 3),       # 10 blocks per row, 12 rows per tile
+    (2, 3, 128, 1500, 8, 0),      # 3 blocks per row, strided, 2-byte stores
+]
+
+
+@pytest.mark.parametrize("tt,hkv,d,n,extra,pos0", LARGE_ENCODE_CASES)
+def test_encode_large_bit_exact(tq, tt, hkv, d, n, extra, pos0):
+    w = synth.scaled(synth.TINY, n_kv_heads=hkv, n_q_heads=hkv, head_dim=d)
+    src = _kv(w, 0, "V", n)
+    wide = np.zeros((n, hkv * d + extra), dtype=np.float16)
+    wide[:, : hkv * d] = src
+    t = torch.from_numpy(wide).to(DEV)[:, : hkv * d]
+    cap = pos0 + n + 5
+    cache = tq.KVCache(tt, hkv, d, capacity_tokens=cap)
+    tq.encode(cache, t, pos0=pos0)
+    assert tq.device_status() == 0
+    rows = cache.buffer.cpu().numpy().reshape(cap, -1)
+    assert np.array_equal(rows[pos0:pos0 + n], oracle.encode_rows(tt, src, hkv, d))
+    assert not rows[:pos0].any() and not rows[pos0 + n:].any()
+
+
+@pytest.mark.parametrize("hkv", [8, 5])
+def test_encode_large_paged_and_out_of_range(tq, hkv):
+    """A prompt written into a paged cache whose pages are scattered, starting inside a
+    page (tiles straddle page boundaries), and one that runs past the last page: its rows
+    beyond are reported and never written, the rest are exact."""
+    w = synth.scaled(synth.BATCHED_PAGED, n_seqs=2, n_kv_heads=hkv, n_q_heads=hkv)
+    cap = 1024
+    pt, n_pages = synth.page_table(w, cap)
+    n = 900
+    src = _kv(w, 0, "K", n)
+    ref = oracle.encode_rows(3, src, hkv, w.head_dim)
+    cache = tq.KVCache(3, hkv, w.head_dim, n_seqs=w.n_seqs, page_tokens=256,
+                       page_table=torch.from_numpy(pt).to(DEV), n_pages=n_pages)
+    all_rows = np.arange(n_pages * 256)
+    for pos0, status in ((101, 0), (203, 7)):   # 203 + 900 > 1024: the last 79 rows are out
+        cache.buffer.zero_()
+        tq.encode(cache, torch.from_numpy(src).to(DEV), seq_id=1, pos0=pos0)
+        assert tq.device_status() == status
+        pool = cache.buffer.cpu().numpy().reshape(n_pages * 256, -1)
+        end = min(pos0 + n, cap)
+        phys = np.array([pt[1, p // 256] * 256 + p % 256 for p in range(pos0, end)])
+        assert np.array_equal(pool[phys], ref[: end - pos0])
+        assert not pool[np.setdiff1d(all_rows, phys)].any()
+
+
 def test_encode_out_of_range_is_reported(tq):
     """A position past the capacity is skipped and reported, never written."""
     cache = tq.KVCache(3, 2, 128, capacity_tokens=4)
