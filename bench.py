@@ -43,7 +43,7 @@ DECODE_STEPS = 128
 # 262,144-token probe of the same kernels (profiles/*_262k.md), scaled to a launch by its
 # token count: attention reads every packed row once, encode reads fp16 and writes packed rows,
 # so traffic grows in proportion to tokens.  None once a kernel changes after its capture.
-TRAFFIC_PER_TOKEN = {"attn": 212.85e6 / 262144, "encode": 627.69e6 / 262144}
+TRAFFIC_PER_TOKEN = {"attn": 212.85e6 / 262144, "encode": 627.06e6 / 262144}
 
 
 def parse():

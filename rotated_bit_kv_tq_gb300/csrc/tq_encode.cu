@@ -159,54 +159,39 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
             x[i + h + 1] = d.y;
         }
     }
-    // ---- 4-5. scale to the unit sphere and take the sign-magnitude Lloyd-Max index,
-    // bit-parallel.  y = fl(z k) with k >= +0, so sign(y) is the sign of z and
-    // |y| = fl(|z| k) (rounding to nearest is symmetric): the magnitudes are scaled in
-    // pairs and the thresholds subtracted in pairs.  "|y| > t" is the sign bit of
-    // fl(t - |y|) (exact zero only when |y| == t, which is not "greater").  Low-plane word
-    // w holds value i = 16w + 8r + k at bits 4k+2r (code bit 0) and 4k+2r+1 (code bit 1):
-    // collecting values in the order j = 2k + r, last first, puts value j's predicate at
-    // bit 2j+1.
+    // ---- 4-5. scale to the unit sphere, y = fl(z k) in pairs, and take the
+    // sign-magnitude Lloyd-Max index, bit-parallel.  "|y| > t" is the sign bit of
+    // fl(t - |y|) (exact zero only when |y| == t, which is not "greater").  The subtraction
+    // is a scalar IEEE operation on the stored y: fed straight from the paired product, it
+    // was evaluated as one fused t - |z| k at full size, which counts a tie whose exact
+    // product lies just above t as "greater".  Low-plane word w holds value
+    // i = 16w + 8r + k at bits 4k+2r (code bit 0) and 4k+2r+1 (code bit 1): collecting
+    // values in the order j = 2k + r, last first, puts value j's predicate at bit 2j+1.
     const float2 kk = make_float2(k, k);
+#pragma unroll
+    for (int i = 0; i < kBlock; i += 2) {
+        const float2 y2 = mul2(make_float2(x[i], x[i + 1]), kk);
+        x[i] = y2.x;
+        x[i + 1] = y2.y;
+    }
     uint32_t W[8], SP[8];
     const float t_lo = TYPE == TQ_TURBO3 ? cb.threshold[4] : cb.threshold[2];
     const float t_mid = TYPE == TQ_TURBO3 ? cb.threshold[5] : 0.0f;
     const float t_hi = TYPE == TQ_TURBO3 ? cb.threshold[6] : 0.0f;
-    const float2 t_lo2 = make_float2(t_lo, t_lo), t_mid2 = make_float2(t_mid, t_mid),
-                 t_hi2 = make_float2(t_hi, t_hi);
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-        float d4[16], d5[16], d6[16];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-#pragma unroll
-            for (int kp = 0; kp < 8; kp += 2) {
-                const int i = 16 * w + 8 * r + kp;
-                const float2 u = mul2(make_float2(fabsf(x[i]), fabsf(x[i + 1])), kk);
-                const float2 a = sub2(t_lo2, u);
-                d4[2 * kp + r] = a.x;
-                d4[2 * kp + 2 + r] = a.y;
-                if (TYPE == TQ_TURBO3) {
-                    const float2 b = sub2(t_mid2, u), c = sub2(t_hi2, u);
-                    d5[2 * kp + r] = b.x;
-                    d5[2 * kp + 2 + r] = b.y;
-                    d6[2 * kp + r] = c.x;
-                    d6[2 * kp + 2 + r] = c.y;
-                }
-            }
-        }
         uint32_t ps = 0, p4 = 0, p5 = 0, p6 = 0;
 #pragma unroll
         for (int j = 15; j >= 0; --j) {
-            ps = collect2(ps, x[16 * w + 8 * (j & 1) + (j >> 1)]);
-            p4 = collect2(p4, d4[j]);
+            const float y = x[16 * w + 8 * (j & 1) + (j >> 1)];
+            const float a = fabsf(y);
+            ps = collect2(ps, y);
+            p4 = collect2(p4, __fsub_rn(t_lo, a));
             if (TYPE == TQ_TURBO3) {
-                p5 = collect2(p5, d5[j]);
-                p6 = collect2(p6, d6[j]);
+                p5 = collect2(p5, __fsub_rn(t_mid, a));
+                p6 = collect2(p6, __fsub_rn(t_hi, a));
             }
         }
-        // z may reach |z| >= 2, whose top exponent bit lands at the even positions
-        ps &= 0xAAAAAAAAu;
         if (TYPE == TQ_TURBO3) {
             // m = (|y|>t4) + (|y|>t5) + (|y|>t6): bit1 = |y|>t5, bit0 = |y|>(bit1 ? t6 : t4);
             // code & 3 = m ^ 3s  -> fields (bit1 ^ s, bit0 ^ s)
@@ -231,14 +216,12 @@ __device__ __forceinline__ void encode_one(const uint8_t *blk_in, int f, uint8_t
         }
     }
     // norm-correction variant: store |x| / |c|, |c| over the same pairwise tree as the norm
-    // (x still holds z here; y = fl(z k) as above)
     uint16_t norm_out = norm16;
     if (cv.norm_correction) {
         float c2[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i)
-            c2[i] = __fadd_rn(code_sq<TYPE>(cb, __fmul_rn(x[i], k)),
-                              code_sq<TYPE>(cb, __fmul_rn(x[i + 64], k)));
+            c2[i] = __fadd_rn(code_sq<TYPE>(cb, x[i]), code_sq<TYPE>(cb, x[i + 64]));
 #pragma unroll
         for (int len = 64; len > 1; len >>= 1)
 #pragma unroll

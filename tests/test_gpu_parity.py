@@ -331,6 +331,20 @@ def test_full_llama_layer_32k_sampled(tq):
     _attn_case(tq, synth.LLAMA3_8B_32K, 3, 3, [32768], layer=5)
 
 
+def test_full_llama_layer_32k_prefill_encode_bit_exact(tq):
+    """The benchmark's prefill call: tq_encode_kv of one Llama-3-8B-shaped layer's K and V
+    over the full 32,768-token context; every packed row equals the oracle's."""
+    w = synth.LLAMA3_8B_32K
+    T = w.ctx
+    k16, v16 = _kv(w, 9, "K", T), _kv(w, 9, "V", T)
+    kc = tq.KVCache(3, w.n_kv_heads, w.head_dim, capacity_tokens=T + 128)
+    vc = tq.KVCache(3, w.n_kv_heads, w.head_dim, capacity_tokens=T + 128)
+    tq.encode_kv(kc, vc, torch.from_numpy(k16).to(DEV), torch.from_numpy(v16).to(DEV))
+    assert tq.device_status() == 0
+    assert np.array_equal(_rows_from(kc, T), oracle.encode_rows(3, k16, w.n_kv_heads, w.head_dim))
+    assert np.array_equal(_rows_from(vc, T), oracle.encode_rows(3, v16, w.n_kv_heads, w.head_dim))
+
+
 def test_full_hd256_layer_128k(tq):
     """One layer of the head_dim-256 workload at its full 131,072-token context."""
     _attn_case(tq, synth.HD256_128K, 2, 2, [131072], layer=1)
