@@ -156,7 +156,7 @@ void oracle_attn_prefill(int type_k, int type_v, const uint8_t *k_rows,
                          double scale, const float *centroids_k, const float *centroids_v,
                          double *out);
 
-/* ---------------------------------------------------------------- variants
+/* ---------------------------------------------------------------- quality variants
  * Quality variants of the method.  NULL selects the plain method everywhere.
  *  - signs: bit i (word i / 32, bit i % 32) negates coordinate i of every block before the
  *    rotation, which becomes W D: a random-sign Hadamard.  [TQ] "What TurboQuant does
