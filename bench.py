@@ -308,8 +308,8 @@ def run_ours(args, rank, world, local_rank, dist):
             tq.attn_decode_append(kc[l], vc[l], new_buf[0, l, 0:1], new_buf[0, l, 1:2],
                                   q_buf[0, l:l + 1], lens_dev, max_len, out_dev[l:l + 1], ws)
     with torch.cuda.graph(g_enc, stream=cap, capture_error_mode="thread_local"):
-        for l in range(L):
-            tq.encode(kc[l], kv_dev[l, 0])
+        for l in range(L):   # the prefill's own call: K and V of one layer in one launch
+            tq.encode_kv(kc[l], vc[l], kv_dev[l, 0], kv_dev[l, 1])
 
     def graph_ms(g, reps=3):
         g.replay()
@@ -386,7 +386,7 @@ def run_ours(args, rank, world, local_rank, dist):
     peak, peak_kind = measured_peak_hbm()
     a_bytes = attn_bytes(w, max_len, tt) + append_bytes(w, tt)
     a_gbs = a_bytes / (attn_launch_ms / 1e3) / 1e9
-    e_bytes = encode_bytes_per_token(w, tt) // 2 * T
+    e_bytes = encode_bytes_per_token(w, tt) * T          # K and V of one layer
     e_gbs = e_bytes / (enc_launch_ms / 1e3) / 1e9
     h2d = kv_host.numel() * 2 + S * (new_host[0].numel() + q_host[0].numel()) * 2
     tpeak, tpeak_kind = measured_peak_tensor()
@@ -419,10 +419,10 @@ def run_ours(args, rank, world, local_rank, dist):
                      "peak_source": peak_kind,
                      "traffic": TRAFFIC_PER_TOKEN["attn"] * max_len if TRAFFIC_PER_TOKEN["attn"] else None,
                      "bytes_per_launch": a_bytes, "launch_ms": attn_launch_ms},
-        "encode_roofline": {"kernel": "tq_encode (prefill, one layer, K)", "bound": "hbm",
+        "encode_roofline": {"kernel": "tq_encode_kv (prefill, one layer, K and V)", "bound": "hbm",
                             "achieved": e_gbs, "peak": peak, "unit": "GB/s", "frac": e_gbs / peak,
                             "peak_source": peak_kind, "bytes_per_launch": e_bytes,
-                            "traffic": TRAFFIC_PER_TOKEN["encode"] * T if TRAFFIC_PER_TOKEN["encode"] else None,
+                            "traffic": 2 * TRAFFIC_PER_TOKEN["encode"] * T if TRAFFIC_PER_TOKEN["encode"] else None,
                             "launch_ms": enc_launch_ms},
         "e2e": {"value": world * n_e2e * S / (e2e_dec_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
