@@ -231,26 +231,43 @@ TQ_API tq_status tq_attn_prefill(const tq_cache *k, const tq_cache *v, const voi
                                  int32_t seq_id, int64_t pos0, int64_t n_q, int n_q_heads,
                                  float softmax_scale, float *out, void *stream);
 
+/* Size of the fixed scratch array of tq_attn_decode_noalloc: 8 MiB per device. */
+#define TQ_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
 /* tq_attn_decode without a workspace argument, for callers that cannot allocate device
  * memory when they need attention.  Examples are code that runs between the steps of
  * a serving loop whose memory pools are fully reserved at start-up, and embedders whose
  * allocator must not be re-entered, or whose policy forbids cudaMalloc (it can
  * synchronise the device) on the decode path.  The pages have no counterpart to this
  * entry point; it is a packaging variant of tq_attn_decode.
- *   Arguments and results are those of tq_attn_decode, minus workspace / ws_bytes.
- *   Scratch: a fixed 8 MiB array in the library's device memory (every GPU that loads
- *   the library holds it until the process exits).  A shape whose
- *   tq_attn_workspace_bytes(...) exceeds 8 MiB returns TQ_ERR_WORKSPACE_TOO_SMALL and
+ *   Arguments and results are those of tq_attn_decode, minus workspace / ws_bytes; the
+ *   argument checks are the same code.
+ *   Scratch: a fixed array of TQ_NOALLOC_SCRATCH_BYTES in the library's device memory
+ *   (every GPU that loads the library holds it until the process exits).  A shape whose
+ *   tq_attn_workspace_bytes(...) exceeds it returns TQ_ERR_WORKSPACE_TOO_SMALL and
  *   launches nothing.  The call never allocates or frees memory.
- *   Set-up: the first call on a device looks up the array's device address (with that
- *   device current); make that first call before any stream capture.
+ *   Set-up: every call looks up the array's device address in the current context (with
+ *   the call's device current), so a device reset or a second context on the device is
+ *   followed.  The first call on a device loads the library's device code there; make
+ *   that first call before any stream capture.
  *   Sharing: all calls on a device share the array and it keeps the last call's
- *   contents.  Calls whose kernels overlap on the GPU (different streams without
- *   ordering) race on it; order them on one stream or with events. */
+ *   contents (each call writes every partial it reads, so nothing needs clearing).
+ *   Calls whose kernels overlap on the GPU (different streams without ordering) race on
+ *   it; order them on one stream or with events. */
 TQ_API tq_status tq_attn_decode_noalloc(const tq_cache *k, const tq_cache *v,
                                         const void *q_f16, int n_seqs, int n_q_heads,
                                         const int32_t *seq_lens, int64_t max_seq_len,
                                         float softmax_scale, float *out, void *stream);
+
+/* Fault injection for tests of the bounded device-side waits: failure detection without a
+ * GPU fault (nothing traps, hangs or touches bad memory).  The next
+ * n_calls launches of the tensor-core decode-attention kernel (tq_attn_decode,
+ * tq_attn_decode_append and tq_attn_decode_noalloc on the shapes that kernel takes) request
+ * no tile copies and give every wait on a tile a limit of 64 polls.  With no copy in flight
+ * each wait runs out, the kernel records TQ_ERR_DEVICE_TIMEOUT for tq_device_status,
+ * writes empty partials (a zero output) and returns normally; later calls run as usual.
+ * Process-wide; n_calls = 0 cancels.  Returns TQ_ERR_INVALID_ARGUMENT for n_calls < 0. */
+TQ_API tq_status tq_inject_wait_timeout(int n_calls);
 
 /* Synchronise `stream`, then read and clear the device status word of the current
  * device: *status_out = TQ_OK or the first device-side error recorded since the

@@ -9,11 +9,13 @@ from __future__ import annotations
 
 import ctypes
 
-from ._lib import (TQ_BLOCK_VALUES, TQ_TURBO2, TQ_TURBO3, TQError, TqCache, check, load)
+from ._lib import (NOALLOC_SCRATCH_BYTES, TQ_BLOCK_VALUES, TQ_TURBO2, TQ_TURBO3, TQError, TqCache,
+                   check, load)
 
-__all__ = ["TQ_TURBO2", "TQ_TURBO3", "TQ_BLOCK_VALUES", "TQError", "TqCache", "KVCache",
+__all__ = ["TQ_TURBO2", "TQ_TURBO3", "TQ_BLOCK_VALUES", "NOALLOC_SCRATCH_BYTES", "TQError", "TqCache", "KVCache",
            "block_bytes", "row_bytes", "codebook_init", "codebook_get", "encode", "encode_kv", "decode",
-           "attn_workspace_bytes", "attn_decode", "attn_prefill", "device_status", "load"]
+           "attn_workspace_bytes", "attn_decode", "attn_decode_append", "attn_prefill",
+           "inject_wait_timeout", "device_status", "load"]
 
 
 def _stream_ptr(stream=None):
@@ -149,6 +151,12 @@ def attn_prefill(k: KVCache, v: KVCache, q, out, *, pos0: int, seq_id: int = 0,
     check(load().tq_attn_prefill(ctypes.byref(k.view), ctypes.byref(v.view), _ptr(q), seq_id,
                                  pos0, n_q, n_q_heads, softmax_scale, _ptr(out),
                                  _stream_ptr(stream)), "tq_attn_prefill")
+
+
+def inject_wait_timeout(n_calls: int):
+    """The next n_calls tensor-core decode-attention launches withhold their tile copies
+    and time out their bounded waits (a test of the failure path; no GPU fault)."""
+    check(load().tq_inject_wait_timeout(n_calls), "tq_inject_wait_timeout")
 
 
 def device_status(stream=None) -> int:

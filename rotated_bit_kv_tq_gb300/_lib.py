@@ -14,6 +14,8 @@ LIB_PATH = os.path.join(_HERE, "libtq.so")
 TQ_TURBO2 = 2
 TQ_TURBO3 = 3
 TQ_BLOCK_VALUES = 128
+# TQ_NOALLOC_SCRATCH_BYTES of tq.h: the fixed scratch of tq_attn_decode_noalloc
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 STATUS_NAMES = {
     0: "TQ_OK", 1: "TQ_ERR_INVALID_ARGUMENT", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_NOT_INITIALIZED",
@@ -83,6 +85,7 @@ SIGNATURES = {
                                        ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                        ctypes.c_int64, ctypes.c_int, ctypes.c_float,
                                        ctypes.c_void_p, ctypes.c_void_p]),
+    "tq_inject_wait_timeout": (ctypes.c_int, [ctypes.c_int]),
     "tq_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }

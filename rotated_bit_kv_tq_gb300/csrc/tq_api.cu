@@ -20,6 +20,49 @@ std::mutex g_mu;
 
 bool valid_type(int type) { return type == TQ_TURBO2 || type == TQ_TURBO3; }
 
+// Worst relative error, over the centroid magnitudes mag[0..n), of the fp16 table scaled by
+// a: |fp16(a m) / a - m| / m (evaluated in double; a is the fp32 value the kernels use).
+double scaled_table_error(float a, const float *mag, int n) {
+    double worst = 0.0;
+    for (int j = 0; j < n; ++j) {
+        const double v = (double)a * (double)mag[j];
+        const double h = (double)__half2float(__double2half(v));
+        const double e = std::fabs(h / (double)a - (double)mag[j]) / (double)mag[j];
+        worst = e > worst ? e : worst;
+    }
+    return worst;
+}
+
+// The scale in [1, 2) that puts every centroid magnitude closest to an fp16 value.  A best
+// scale puts at least one magnitude exactly on an fp16 value, so the candidates are
+// a = g / m_j for every magnitude m_j and every fp16 value g with a in [1, 2); the first
+// candidate with the smallest worst-case error wins (a deterministic search over at most
+// 4 x 2048 candidates).
+float choose_h_scale(const float *centroid, int levels) {
+    float mag[4];
+    const int n = levels / 2;
+    for (int j = 0; j < n; ++j) mag[j] = centroid[levels / 2 + j];
+    float best = 1.0f;
+    double best_err = scaled_table_error(1.0f, mag, n);
+    for (int j = 0; j < n; ++j) {
+        // fp16 values g in [m_j, 2 m_j): every mantissa of the one or two binades involved
+        for (int e = -15; e <= 15; ++e) {
+            for (int m = 0; m < 1024; ++m) {
+                const double g = std::ldexp(1.0 + m / 1024.0, e);
+                const double a = g / (double)mag[j];
+                if (a < 1.0 || a >= 2.0) continue;
+                const float af = (float)a;
+                const double err = scaled_table_error(af, mag, n);
+                if (err < best_err) {
+                    best_err = err;
+                    best = af;
+                }
+            }
+        }
+    }
+    return best;
+}
+
 const Codebook &host_codebook(int type) {
     int i = cb_index(type);
     if (!g_host_cb_done[i]) {
@@ -28,10 +71,10 @@ const Codebook &host_codebook(int type) {
         solve_codebook(levels, c);
         Codebook cb;
         std::memset(&cb, 0, sizeof cb);
-        for (int j = 0; j < levels; ++j) {
-            cb.centroid[j] = (float)c[j];
-            cb.centroid_h[j] = __float2half_rn(cb.centroid[j]);
-        }
+        for (int j = 0; j < levels; ++j) cb.centroid[j] = (float)c[j];
+        cb.h_scale = choose_h_scale(cb.centroid, levels);
+        for (int j = 0; j < levels; ++j)
+            cb.centroid_h[j] = __double2half((double)cb.h_scale * (double)cb.centroid[j]);
         // fp32 midpoints of the fp32 centroids
         for (int j = 0; j + 1 < levels; ++j)
             cb.threshold[j] = (cb.centroid[j] + cb.centroid[j + 1]) * 0.5f;
@@ -42,6 +85,12 @@ const Codebook &host_codebook(int type) {
 }
 
 }  // namespace
+
+float centroid_h_scale(int type) {
+    if (!valid_type(type)) return 1.0f;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return host_codebook(type).h_scale;
+}
 
 bool codebook_ready(int type, int device) {
     if (device < 0 || device >= kMaxDevices || !valid_type(type)) return false;
@@ -198,12 +247,11 @@ size_t tq_attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t 
 
 }  // extern "C"
 
-namespace {
-// Argument checks shared by tq_attn_decode and tq_attn_decode_append.
-tq_status attn_decode_checked(const tq_cache *k, const tq_cache *v, const void *q_f16, int n_seqs,
-                              int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
-                              float softmax_scale, float *out, void *workspace, size_t ws_bytes,
-                              void *stream, const void *k_new, const void *v_new) {
+namespace tq {
+
+tq_status check_attn_args(const tq_cache *k, const tq_cache *v, const void *q_f16, int n_seqs,
+                          int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
+                          float softmax_scale, const float *out, float *scale_out) {
     tq_status st = validate_cache(k);
     if (st != TQ_OK) return st;
     st = validate_cache(v);
@@ -218,12 +266,27 @@ tq_status attn_decode_checked(const tq_cache *k, const tq_cache *v, const void *
     if (reinterpret_cast<uintptr_t>(q_f16) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
         return TQ_ERR_INVALID_ARGUMENT;
     if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale)) return TQ_ERR_INVALID_ARGUMENT;
-    if (softmax_scale == 0.0f) softmax_scale = 1.0f / std::sqrt((float)k->head_dim);
+    *scale_out = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)k->head_dim) : softmax_scale;
+    return TQ_OK;
+}
+
+}  // namespace tq
+
+namespace {
+// tq_attn_decode and tq_attn_decode_append: the shared checks, then the workspace's.
+tq_status attn_decode_checked(const tq_cache *k, const tq_cache *v, const void *q_f16, int n_seqs,
+                              int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
+                              float softmax_scale, float *out, void *workspace, size_t ws_bytes,
+                              void *stream, const void *k_new, const void *v_new) {
+    float scale = 0.0f;
+    tq_status st = check_attn_args(k, v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len,
+                                   softmax_scale, out, &scale);
+    if (st != TQ_OK) return st;
     size_t need = tq_attn_workspace_bytes(n_seqs, n_q_heads, k->head_dim, max_seq_len);
     if (need > 0 && (!workspace || ws_bytes < need)) return TQ_ERR_WORKSPACE_TOO_SMALL;
     if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16) return TQ_ERR_INVALID_ARGUMENT;
-    return launch_attn(*k, *v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len, softmax_scale,
-                       out, workspace, ws_bytes, static_cast<cudaStream_t>(stream), k_new, v_new);
+    return launch_attn(*k, *v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len, scale, out,
+                       workspace, ws_bytes, static_cast<cudaStream_t>(stream), k_new, v_new);
 }
 }  // namespace
 

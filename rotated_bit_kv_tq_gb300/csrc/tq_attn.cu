@@ -477,32 +477,20 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
 // Allocation-free variant of tq_attn_decode.  The split partials live in a fixed
 // file-scope device array instead of a caller-provided workspace.
 // ---------------------------------------------------------------------------------
-#include <cmath>
-#include <mutex>
-
 namespace tq {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
+constexpr size_t kStaticScratchBytes = TQ_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];
 
-constexpr int kMaxScratchDevices = 64;
-void *g_scratch_addr[kMaxScratchDevices];
-std::mutex g_scratch_mu;
-
-// Device address of g_attn_scratch on the current device (looked up once per device;
-// the host-side name of the array is only a stand-in and must never reach a kernel).
+// Device address of g_attn_scratch in the current device's context.  It is looked up on
+// every call rather than cached: after cudaDeviceReset, or in another context on the same
+// device, the library's device code is loaded anew and the array may move.  (The host-side
+// name of the array is only a stand-in and must never reach a kernel.)
 tq_status scratch_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxScratchDevices) return TQ_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
+    *out = p;
     return TQ_OK;
 }
 
@@ -514,21 +502,10 @@ extern "C" tq_status tq_attn_decode_noalloc(const tq_cache *k, const tq_cache *v
                                              const int32_t *seq_lens, int64_t max_seq_len,
                                              float softmax_scale, float *out, void *stream) {
     using namespace tq;
-    tq_status st = validate_cache(k);
+    float scale = 0.0f;
+    tq_status st = check_attn_args(k, v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len,
+                                   softmax_scale, out, &scale);
     if (st != TQ_OK) return st;
-    st = validate_cache(v);
-    if (st != TQ_OK) return st;
-    if (k->n_kv_heads != v->n_kv_heads || k->head_dim != v->head_dim)
-        return TQ_ERR_INVALID_ARGUMENT;
-    if (n_seqs < 1 || n_seqs > k->n_seqs || n_seqs > v->n_seqs) return TQ_ERR_INVALID_ARGUMENT;
-    if (n_q_heads < 1 || n_q_heads % k->n_kv_heads) return TQ_ERR_INVALID_ARGUMENT;
-    if (n_q_heads / k->n_kv_heads > 16 || n_q_heads > 128) return TQ_ERR_UNSUPPORTED;
-    if (max_seq_len < 0 || max_seq_len > ((int64_t)1 << 31) - 1) return TQ_ERR_INVALID_ARGUMENT;
-    if (!q_f16 || !seq_lens || !out) return TQ_ERR_INVALID_ARGUMENT;
-    if (reinterpret_cast<uintptr_t>(q_f16) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
-        return TQ_ERR_INVALID_ARGUMENT;
-    if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale)) return TQ_ERR_INVALID_ARGUMENT;
-    if (softmax_scale == 0.0f) softmax_scale = 1.0f / std::sqrt((float)k->head_dim);
     // The shape must fit the fixed array; larger shapes are refused, never truncated.
     const size_t need = attn_workspace_bytes(n_seqs, n_q_heads, k->head_dim, max_seq_len,
                                              device_sm_count());
@@ -538,6 +515,6 @@ extern "C" tq_status tq_attn_decode_noalloc(const tq_cache *k, const tq_cache *v
     if (st != TQ_OK) return st;
     // Every partial the merge reads is written by the same call first, so nothing in
     // the array needs clearing between calls.
-    return launch_attn(*k, *v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len, softmax_scale,
-                       out, scratch, kStaticScratchBytes, static_cast<cudaStream_t>(stream));
+    return launch_attn(*k, *v, q_f16, n_seqs, n_q_heads, seq_lens, max_seq_len, scale, out,
+                       scratch, kStaticScratchBytes, static_cast<cudaStream_t>(stream));
 }

@@ -19,10 +19,18 @@
 // shared memory; the probabilities move from the score accumulators to the value
 // operand with movmatrix (an 8x8 transpose across the warp).
 //
-// Data movement: one CTA per (split, sequence), 8 warps; warp w owns KV head w % Hkv and a
-// 64-token slice of every tile.  Tiles of whole packed rows (all KV heads) are copied by
-// TMA bulk copies (one per contiguous run of rows, split at page boundaries) into a ring
-// of shared-memory stages completed through mbarriers; waits are bounded.
+// Operand precision: the rotated query is held as an fp16 pair q~ = hi + lo (lo the fp16
+// rounding of the remainder), and the centroid tables are scaled so that their fp16 values
+// are nearly exact (Codebook::h_scale, divided out in fp32).  With at most four query heads
+// per KV head the low halves sit in the four otherwise empty columns of the score MMA, so
+// they cost no extra MMA; with more, a second MMA per k-step adds them.
+//
+// Data movement: one CTA per (split, sequence), one CTA per SM; warp w owns KV head w % Hkv,
+// and the warps of one KV head take consecutive 32-row slices of each half of every tile.
+// Tiles of whole packed rows (all KV heads) are copied by TMA bulk copies (one per
+// contiguous run of rows, split at page boundaries) into a ring of shared-memory stages
+// completed through mbarriers; waits are bounded.
+#include <atomic>
 #include <cmath>
 
 #include "tq_internal.cuh"
@@ -43,15 +51,20 @@ constexpr int kWarpTokens = 64;            // 4 m-tiles of 16 tokens per warp pe
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kWaitLimit = 1u << 26;  // bounded mbarrier wait (tens of ms)
-constexpr size_t kSmemBudget = 220 * 1024;   // per CTA (one per SM)
+constexpr uint32_t kInjectedWaitLimit = 64;   // polls per wait under tq_inject_wait_timeout
+
+// Launches still to run with injected timeouts (tq_inject_wait_timeout).
+std::atomic<int> g_inject_timeouts{0};
+constexpr size_t kSmemBudget = 227 * 1024;   // per CTA (one per SM): the sm_100 family's maximum
 
 // Rotated queries in shared memory, in MMA-fragment order: head h, block b, k-step j and
-// lane quarter q4 hold the four values 32 q4 + 4j .. +3 at halfs h*QS + 128 b + 16 j + 4 q4.
-// QS = 128 nb + 16 puts consecutive heads 8 banks apart, so the 8-byte B-fragment loads of
-// four heads x four quarters cover all 32 banks once (eight heads: two wavefronts).
+// lane quarter q4 hold the four values 32 q4 + 4j .. +3 at halfs h*QS + 128 b + 16 j + 4 q4
+// (the high fp16 parts; the low parts follow in the same layout, Hq * QS halfs later).
+// QS = 128 nb + 16 puts consecutive heads 8 banks apart, so each half-warp's 8-byte
+// B-fragment loads (four heads x four quarters) cover all 32 banks once.
 __host__ __device__ constexpr int q_stride(int nb) { return 128 * nb + 16; }
 inline size_t q_bytes(int n_q_heads, int nb) {
-    return ((size_t)n_q_heads * q_stride(nb) * 2 + 127) & ~size_t(127);
+    return ((size_t)2 * n_q_heads * q_stride(nb) * 2 + 127) & ~size_t(127);
 }
 
 struct MmaParams {
@@ -60,7 +73,8 @@ struct MmaParams {
     const __half *k_new, *v_new;   // decode-step append: [n_seqs][Hkv][D] fp16, or null
     const int32_t *seq_lens;
     float *part;        // [n_seqs][n_splits][Hq][part_stride(D)]
-    float score_scale;  // softmax scale * log2(e) / sqrt(128)
+    float score_scale;  // softmax scale * log2(e) / (sqrt(128) * h_scale of the K table)
+    float v_unscale;    // 1 / h_scale of the V table (applied to the value norms)
     int64_t max_len;
     int32_t n_q_heads, n_kv_heads, group, head_dim;
     int32_t n_splits, tokens_per_split;
@@ -69,6 +83,8 @@ struct MmaParams {
     int32_t stages;
     int32_t stage_bytes;
     int32_t cpart_offset;   // bytes from the first stage to this CTA's partial rows
+    uint32_t wait_limit;    // polls per bounded mbarrier wait
+    int32_t withhold_tiles; // fault injection: request no tile copies (every tile wait runs out)
     // 2, 4, 2^16, 2^30, 2^31: shift amounts as multipliers passed at run time, so that the
     // selector shifts compile to integer multiply-adds (FMA pipe) instead of ALU shifts
     uint32_t mul2, mul4, hi16, hi30, hi31;
@@ -136,15 +152,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Bounded wait on an mbarrier phase; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t it = 0; it < limit; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
 
 // APPEND: the decode-step form (p.k_new set); a separate instantiation, so that the plain
-// attention carries none of its code.
-template <int TK, int TV, int NB, bool APPEND>
+// attention carries none of its code.  QLO2: more than four query heads per KV head, so the
+// low parts of the query take a second MMA per k-step instead of the spare columns.
+template <int TK, int TV, int NB, bool APPEND, bool QLO2>
 __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const MmaParams p) {
     constexpr int kConsumers = consumers(NB);
     extern __shared__ __align__(128) uint8_t smem[];
@@ -158,7 +175,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
 
     constexpr int QS = q_stride(NB);
     __half *qh = reinterpret_cast<__half *>(smem);                          // [Hq][QS]
-    const size_t qbytes = ((size_t)Hq * QS * 2 + 127) & ~size_t(127);
+    const size_t qbytes = ((size_t)2 * Hq * QS * 2 + 127) & ~size_t(127);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + qbytes);          // [stages]
     uint64_t *empty = full + 4;                                            // [stages]
     uint8_t *stage0 = smem + qbytes + 128;
@@ -213,14 +230,16 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     // per call, against 24.4 with warp 0 rotating too and 25.6 with every stage requested
     // after the rotation).
     auto issue = [&](int i) {
+        if (p.withhold_tiles) return;   // injected fault: nothing is copied, no copy in flight
         const int64_t t0 = tile_start(i);
         const int nt = tile_len(i) - (i == i_new && new_in_stage ? 1 : 0);
         uint8_t *dk = stage0 + (size_t)(i % p.stages) * p.stage_bytes;
         issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i % p.stages]));
     };
     if (tid == 0 && n_tiles > 0) issue(0);
-    // ---- rotate q once per call: qh = fp16(W q_b * scale * log2(e) / sqrt(128)) by warps
-    // 1-15; a warp loads its (up to five) query blocks at once, then rotates them
+    // ---- rotate q once per call: y = W q_b * score_scale, stored as hi = fp16(y) and
+    // lo = fp16(y - hi), by warps 1-15; a warp loads its (up to five) query blocks at once,
+    // then rotates them
     constexpr int kRot = kConsumers - 1;
     if (warp > 0)
     for (int hb0 = warp - 1; hb0 < Hq * NB; hb0 += 5 * kRot) {
@@ -243,11 +262,13 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             float v[4] = {f01.x, f01.y, f23.x, f23.y};
             apply_signs4(v, p.kc, 4 * lane);   // rotation W D of the K cache
             warp_fwht4(v, lane);
-            uint2 o;
-            o.x = pack_half2(v[0] * p.score_scale, v[1] * p.score_scale);
-            o.y = pack_half2(v[2] * p.score_scale, v[3] * p.score_scale);
+            uint2 hi, lo;
+            split_half2(v[0] * p.score_scale, v[1] * p.score_scale, hi.x, lo.x);
+            split_half2(v[2] * p.score_scale, v[3] * p.score_scale, hi.y, lo.y);
             // lane = 8 q4 + j holds values 4 lane .. 4 lane + 3 = 32 q4 + 4 j ..
-            *reinterpret_cast<uint2 *>(qh + h * QS + b * kBlock + 16 * (lane & 7) + 4 * (lane >> 3)) = o;
+            __half *dst = qh + h * QS + b * kBlock + 16 * (lane & 7) + 4 * (lane >> 3);
+            *reinterpret_cast<uint2 *>(dst) = hi;
+            *reinterpret_cast<uint2 *>(dst + Hq * QS) = lo;
         }
     }
     if (tid == 0)   // no copy in this loop reads the new row (see above)
@@ -298,12 +319,20 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             for (int e = 0; e < 4; ++e) oacc[b][j][e] = 0.f;
 
     {
-        // B fragments of the rotated query (head n = g8 of KV head g, values 32q4 + 4j + e)
-        // are read from shared memory at each use: one 8-byte load per k-step.
-        const bool qv = g8 < G;
-        const __half *qrow = qh + (g * G + (qv ? g8 : 0)) * QS + 4 * q4;
+        // B fragments of the rotated query (column n = g8, values 32q4 + 4j + e) are read
+        // from shared memory at each use: one 8-byte load per k-step and part.  Without
+        // QLO2, column n < 4 holds the high part of head n and column 4 + n its low part;
+        // with QLO2, column n holds head n, high part in the first MMA, low in the second.
+        const int qhead = QLO2 ? g8 : (g8 & 3);
+        const bool qv = qhead < G;
+        const __half *qrow = qh + ((QLO2 || g8 < 4 ? 0 : Hq) + g * G + (qv ? qhead : 0)) * QS + 4 * q4;
+        const __half *qrow_lo = qrow + Hq * QS;
         auto bq = [&](int b, int j) -> uint2 {
             const uint2 v = *reinterpret_cast<const uint2 *>(qrow + b * kBlock + 16 * j);
+            return qv ? v : make_uint2(0u, 0u);
+        };
+        auto bq_lo = [&](int b, int j) -> uint2 {
+            const uint2 v = *reinterpret_cast<const uint2 *>(qrow_lo + b * kBlock + 16 * j);
             return qv ? v : make_uint2(0u, 0u);
         };
         HalfTables tk, tv;
@@ -341,7 +370,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
 
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % p.stages;
-            if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((i / p.stages) & 1))) {
+            if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((i / p.stages) & 1), p.wait_limit)) {
                 record_error(TQ_ERR_DEVICE_TIMEOUT);
                 timed_out = true;
                 break;
@@ -394,6 +423,11 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                                 const uint2 q0 = bq(b, j), q1 = bq(b, j + 1);
                                 mma16816(acc[0], xa[0], xb[0], xa[1], xb[1], q0.x, q0.y);
                                 mma16816(acc[1], xa[2], xb[2], xa[3], xb[3], q1.x, q1.y);
+                                if (QLO2) {
+                                    const uint2 l0 = bq_lo(b, j), l1 = bq_lo(b, j + 1);
+                                    mma16816(acc[0], xa[0], xb[0], xa[1], xb[1], l0.x, l0.y);
+                                    mma16816(acc[1], xa[2], xb[2], xa[3], xb[3], l1.x, l1.y);
+                                }
                             }
                         const float nA = kn[mt][b][0], nB = kn[mt][b][1];
                         s0 = fmaf(nA, acc[0][0] + acc[1][0], s0);
@@ -404,6 +438,12 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                         for (int c = 0; c < 2; ++c)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+                    }
+                    if (!QLO2) {   // add the low parts' columns 4 + n (lane q4 ^ 2)
+                        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+                        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+                        s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+                        s3 += __shfl_xor_sync(0xffffffffu, s3, 2);
                     }
                     // rows past the tile's valid tokens hold stale bytes: masked here
                     const bool okA = rA < nt, okB = rB < nt;
@@ -464,8 +504,9 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                             const int row = hr0 + 16 * mt + g8 + 8 * t;
                             const uint8_t *rv = Vt + (size_t)row * Rv;
                             vq[mt][b][t] = load_quarter<TV>(rv, owv[b], ovv[b], shv[b]);
-                            // masked rows may hold stale bytes: their weight is forced to 0
-                            vn[mt][b][t] = row < nt ? ld_norm(rv + (g * NB + b) * BV) : 0.f;
+                            // masked rows may hold stale bytes: their weight is forced to 0;
+                            // 1 / h_scale undoes the scaled V table
+                            vn[mt][b][t] = row < nt ? ld_norm(rv + (g * NB + b) * BV) * p.v_unscale : 0.f;
                         }
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
@@ -497,7 +538,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
             // refill: once every warp has released stage s, bring in tile i + stages
             if (tid == 0 && i + p.stages < n_tiles) {
-                if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)((i / p.stages) & 1))) {
+                if (!mbar_wait(smem_u32(&empty[s]), (uint32_t)((i / p.stages) & 1), p.wait_limit)) {
                     record_error(TQ_ERR_DEVICE_TIMEOUT);
                 } else {
                     uint8_t *dk = stage0 + (size_t)s * p.stage_bytes;
@@ -659,11 +700,11 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-template <int TK, int TV, int NB, bool APPEND>
+template <int TK, int TV, int NB, bool APPEND, bool QLO2>
 tq_status launch_tt(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     const size_t qbytes = q_bytes(p.n_q_heads, NB);
     const size_t smem = qbytes + 128 + (size_t)p.stages * p.stage_bytes;
-    if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB, APPEND>,
+    if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB, APPEND, QLO2>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return TQ_ERR_CUDA;
     PdlConfig lc(dim3(p.n_splits, n_seqs), dim3(32 * consumers(NB)), smem, stream);
@@ -672,13 +713,16 @@ tq_status launch_tt(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     lc.attrs[1].val.clusterDim.y = 1;
     lc.attrs[1].val.clusterDim.z = 1;
     lc.cfg.numAttrs = 2;
-    return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_mma_kernel<TK, TV, NB, APPEND>, p));
+    return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_mma_kernel<TK, TV, NB, APPEND, QLO2>, p));
 }
 
 template <int TK, int TV, int NB>
 tq_status launch_t(const MmaParams &p, int n_seqs, cudaStream_t stream) {
-    return p.k_new ? launch_tt<TK, TV, NB, true>(p, n_seqs, stream)
-                   : launch_tt<TK, TV, NB, false>(p, n_seqs, stream);
+    if (p.group > 4)
+        return p.k_new ? launch_tt<TK, TV, NB, true, true>(p, n_seqs, stream)
+                       : launch_tt<TK, TV, NB, false, true>(p, n_seqs, stream);
+    return p.k_new ? launch_tt<TK, TV, NB, true, false>(p, n_seqs, stream)
+                   : launch_tt<TK, TV, NB, false, false>(p, n_seqs, stream);
 }
 
 template <int NB>
@@ -720,7 +764,8 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     p.v_new = static_cast<const __half *>(v_new);
     p.seq_lens = seq_lens;
     p.part = part;
-    p.score_scale = scale * kLog2e * kInvSqrt128;
+    p.score_scale = scale * kLog2e * kInvSqrt128 / centroid_h_scale(k.type);
+    p.v_unscale = 1.0f / centroid_h_scale(v.type);
     p.max_len = max_seq_len;
     p.n_q_heads = n_q_heads;
     p.n_kv_heads = k.n_kv_heads;
@@ -731,6 +776,14 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     const int nb = k.head_dim / kBlock;
     p.wph = consumers(nb) / k.n_kv_heads;
     p.tile_tokens = kWarpTokens * p.wph;
+    p.wait_limit = kWaitLimit;
+    p.withhold_tiles = 0;
+    for (int n = g_inject_timeouts.load(); n > 0;)
+        if (g_inject_timeouts.compare_exchange_weak(n, n - 1)) {
+            p.wait_limit = kInjectedWaitLimit;
+            p.withhold_tiles = 1;
+            break;
+        }
     p.mul2 = 2u;
     p.mul4 = 4u;
     p.hi16 = 1u << 16;
@@ -749,4 +802,12 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
                    : launch_nb<2>(k.type, v.type, p, n_seqs, stream);
 }
 
+tq_status inject_wait_timeout(int n_calls) {
+    if (n_calls < 0) return TQ_ERR_INVALID_ARGUMENT;
+    g_inject_timeouts.store(n_calls);
+    return TQ_OK;
+}
+
 }  // namespace tq
+
+extern "C" tq_status tq_inject_wait_timeout(int n_calls) { return tq::inject_wait_timeout(n_calls); }

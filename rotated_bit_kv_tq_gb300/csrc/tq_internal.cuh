@@ -134,7 +134,13 @@ struct PdlConfig {
 struct Codebook {
     float centroid[8];
     float threshold[7];
-    __half centroid_h[8];  // fp16 copies used by the tensor-core attention path
+    // fp16 operands of the tensor-core attention kernels: centroid_h[j] = fp16(h_scale *
+    // centroid[j]), with h_scale in [1, 2) chosen so that every scaled centroid lies within
+    // a few 1e-5 (relative) of an fp16 value.  The kernels divide h_scale out in fp32 (the
+    // query scale on the key side, the value norms on the value side), so a centroid's
+    // systematic fp16 error drops from up to 2.3e-4 to 2.2e-5 (turbo3) and 7e-7 (turbo2).
+    __half centroid_h[8];
+    float h_scale;
 };
 #if defined(__CUDACC__)
 extern __constant__ Codebook c_codebook[2];
@@ -148,6 +154,12 @@ tq_status check_cuda(cudaError_t e);
 int device_sm_count();
 CacheView make_view(const tq_cache &c);
 tq_status validate_cache(const tq_cache *c);
+// Argument checks of the single-token attention entry points (tq_attn_decode,
+// tq_attn_decode_append, tq_attn_decode_noalloc), everything but the scratch memory; on
+// success *scale_out is the softmax scale to use (1/sqrt(head_dim) when 0 is passed).
+tq_status check_attn_args(const tq_cache *k, const tq_cache *v, const void *q_f16, int n_seqs,
+                          int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len,
+                          float softmax_scale, const float *out, float *scale_out);
 
 // Kernel launchers (one per .cu file).
 tq_status launch_encode(const tq_cache &dst, const void *src, int64_t n_tokens, int64_t stride,
@@ -177,11 +189,17 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
                           float *part, int n_splits, int tokens_per_split, const void *k_new,
                           const void *v_new, cudaStream_t stream);
 
+// Fault injection of tq_inject_wait_timeout (tq_attn_mma.cu).
+tq_status inject_wait_timeout(int n_calls);
+
 // Prompt-chunk attention on the 5th-generation tensor cores (tq_prefill_tc.cu).
 bool prefill_supported(const tq_cache &k, const tq_cache &v, int n_q_heads);
 tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, int32_t seq_id,
                          int64_t pos0, int64_t n_q, int n_q_heads, float scale, float *out,
                          cudaStream_t stream);
+
+// h_scale of a type's fp16 centroid table (see Codebook); 1 for an unknown type.
+float centroid_h_scale(int type);
 
 // Host Lloyd-Max solver (tq_codebook.cpp).
 void solve_codebook(int levels, double *centroids);

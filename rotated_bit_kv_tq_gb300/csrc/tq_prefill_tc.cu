@@ -23,7 +23,9 @@
 //    centroids, keys x coords, K-major, norms apart; V: |v| times centroids, keys x coords
 //    with coords contiguous, MN-major), double-buffered;
 //  - warp 16: allocates TMEM and issues the MMAs from one thread, in whichever order their
-//    inputs become ready: S[b] = Q~ K^T (M = 128 rows, N = 128 keys, K = 128 coords) into
+//    inputs become ready: S[b] = Q~ K^T (M = 128 rows, N = 128 keys, K = 128 coords; Q~ is
+//    an fp16 pair hi + lo, two MMAs per k-step, and the centroid table is scaled to be nearly
+//    exact in fp16, Codebook::h_scale) into
 //    one of two TMEM score buffers, and O += P V with P read from one of two TMEM buffers
 //    (N = 128 coords, K = 128 keys); completions arrive on mbarriers through
 //    tcgen05.commit.
@@ -81,11 +83,13 @@ struct TcParams {
     int32_t n_kv_heads;
     int64_t n_qblocks;      // query blocks of bq tokens
     int32_t chunked_k, chunked_v;
-    float score_scale;      // softmax scale * log2(e) / sqrt(128)
+    float score_scale;      // softmax scale * log2(e) / (sqrt(128) * h_scale of the K table)
+    float out_scale;        // 1 / (sqrt(128) * h_scale of the V table)
 };
 
 struct TcSmem {
-    alignas(1024) uint8_t q[32768];        // Q~ [row][coord], K-major
+    alignas(1024) uint8_t q[32768];        // Q~ high fp16 parts [row][coord], K-major
+    alignas(1024) uint8_t ql[32768];       // Q~ low parts (fp16 rounding of the remainder)
     alignas(1024) uint8_t k[2][32768];     // K tile [key][coord], K-major
     alignas(1024) uint8_t v[2][32768];     // V tile [key][coord], coords contiguous (MN-major)
     alignas(16) uint8_t raw[2][kTcKeys * 64];   // staged blocks of one tile (K, V), word-major
@@ -454,13 +458,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
 #pragma unroll
                 for (int i = 0; i < 64; ++i) x[i] = 0.f;
             }
+            // Q~ = hi + lo, both fp16: the scores take both (two MMAs per k-step), so the
+            // query keeps about 22 bits
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
+                uint32_t w[4], wl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    w[e] = pack_half2(x[8 * c + 2 * e] * p.score_scale, x[8 * c + 2 * e + 1] * p.score_scale);
+                    split_half2(x[8 * c + 2 * e] * p.score_scale, x[8 * c + 2 * e + 1] * p.score_scale, w[e], wl[e]);
                 *reinterpret_cast<uint4 *>(sm.q + canon(r, 64 * h + 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(sm.ql + canon(r, 64 * h + 8 * c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -571,7 +578,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         named_sync(pair_bar, 64);
         const float l_row = l_run + sm.xch[n_tiles & 1][h ^ 1][r];
         if (valid && done) {
-            const float inv = l_row > 0.f ? kInvSqrt128 / l_row : 0.f;
+            const float inv = l_row > 0.f ? p.out_scale / l_row : 0.f;
             float4 *dst = reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)kBlock + 64 * h);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
@@ -595,7 +602,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
     } else if (lane == 0) {
         // ================= MMA issue (one thread)
         constexpr uint32_t idesc_s = idesc_f16(false), idesc_pv = idesc_f16(true);
-        const uint32_t q_base = smem_u32(sm.q);
+        const uint32_t q_base = smem_u32(sm.q), ql_base = smem_u32(sm.ql);
         bool ok = tc_wait(bar(kBarQ), 0);
         // issue S(ns) and P V(npv) in whichever order their inputs become ready: S(i + 1)
         // must not hold back P V(i) while tile i + 1 is still being decoded
@@ -613,6 +620,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
                     for (int ks = 0; ks < 8; ++ks)
                         tc_mma(tmem + 128u * b, sdesc(q_base + 256u * ks, 128, 2048),
                                sdesc(k_base + 256u * ks, 128, 2048), idesc_s, ks > 0);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)   // the low parts of the query
+                        tc_mma(tmem + 128u * b, sdesc(ql_base + 256u * ks, 128, 2048),
+                               sdesc(k_base + 256u * ks, 128, 2048), idesc_s, 1u);
                     tc_commit(bar(kBarSFull + b));
                     ++ns;
                     progressed = true;
@@ -686,7 +697,10 @@ tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, in
     p.bq = kTcRows / p.group;
     p.chunked_k = p.kc.row_bytes % 16 == 0;
     p.chunked_v = p.vc.row_bytes % 16 == 0;
-    p.score_scale = scale * kTcLog2e * kInvSqrt128;
+    // the fp16 centroid tables are scaled by h_scale (Codebook); the query scale divides the
+    // K table's out, the output scale the V table's
+    p.score_scale = scale * kTcLog2e * kInvSqrt128 / centroid_h_scale(k.type);
+    p.out_scale = kInvSqrt128 / centroid_h_scale(v.type);
     p.n_kv_heads = k.n_kv_heads;
     p.n_qblocks = (n_q + p.bq - 1) / p.bq;
     const int64_t n_ctas = p.n_qblocks * k.n_kv_heads;

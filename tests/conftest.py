@@ -16,3 +16,19 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Largest per-(query, head) attention error of every GPU parity check, by label."""
+    from attn_check import RECORDS
+    if not RECORDS:
+        return
+    worst = {}
+    for label, per, whole in RECORDS:
+        key = label.split("#")[0]
+        w = worst.get(key, (0.0, 0.0, 0))
+        worst[key] = (max(w[0], per), max(w[1], whole), w[2] + 1)
+    terminalreporter.write_sep("-", "attention error per (query, head) vector, worst per label")
+    for key in sorted(worst):
+        per, whole, n = worst[key]
+        terminalreporter.write_line(f"{key:60s} per-head max {per:.3e}  whole max {whole:.3e}  ({n} checks)")

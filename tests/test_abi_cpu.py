@@ -67,3 +67,18 @@ def test_host_validation_without_gpu(lib):
     assert lib.tq_status_str(4) == b"TQ_ERR_WORKSPACE_TOO_SMALL"
     assert lib.tq_status_str(99) == b"TQ_UNKNOWN_STATUS"
     assert lib.tq_device_status(None, None) == 1
+
+
+def test_noalloc_scratch_size_matches_header():
+    """The binding's NOALLOC_SCRATCH_BYTES is the header's TQ_NOALLOC_SCRATCH_BYTES."""
+    from rotated_bit_kv_tq_gb300 import NOALLOC_SCRATCH_BYTES
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    m = re.search(r"#define\s+TQ_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m, "TQ_NOALLOC_SCRATCH_BYTES not found in tq.h"
+    assert NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_inject_wait_timeout_arguments(lib):
+    """Host-only: a negative count is refused; 0 cancels (no kernel is involved)."""
+    assert lib.tq_inject_wait_timeout(-1) == 1
+    assert lib.tq_inject_wait_timeout(0) == 0

@@ -17,7 +17,7 @@ from rotated_bit_kv_tq_gb300 import synth
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-ATTN_TOL = 2e-3
+from attn_check import assert_attn_close  # noqa: E402
 DEV = "cuda"
 MASK_K = 0x9E3779B97F4A7C15F39CC0605CEDC834
 MASK_V = 0x2545F4914F6CDD1D94D049BB133111EB
@@ -105,8 +105,7 @@ def _append_case(tq, w, tk, tv, lens, *, layer=0, paged=False, cap=None, var=Non
         vr = oracle.encode_rows(tv, vs[s], Hkv, D, var=vvar)
         ref = oracle.attn_decode(tk, tv, kr, vr, q16[s], L, Hq, Hkv, D, 1.0 / np.sqrt(D),
                                  var_k=kvar, var_v=vvar)
-        err = np.linalg.norm(o[s] - ref) / np.linalg.norm(ref)
-        assert err < ATTN_TOL, (s, L, err)
+        assert_attn_close(o[s], ref, f"append {w.name} turbo{tk}/{tv}#s{s} L{L}")
 
 
 @pytest.mark.parametrize("tk,tv", [(3, 3), (2, 2), (3, 2), (2, 3)])

@@ -15,7 +15,8 @@ from rotated_bit_kv_tq_gb300 import synth
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-ATTN_TOL = 2e-3
+from attn_check import ATTN_TOL, assert_attn_close  # noqa: E402
+
 DECODE_TOL = 1e-3
 
 
@@ -248,9 +249,7 @@ def _attn_case(tq, w, tk, tv, lens, layer=0, paged=False, cap=None):
         if L == 0:
             assert np.all(o[s] == 0.0)
             continue
-        err = np.linalg.norm(o[s] - ref) / np.linalg.norm(ref)
-        errs.append(err)
-        assert err < ATTN_TOL, (s, L, err)
+        errs.append(assert_attn_close(o[s], ref, f"decode {w.name} turbo{tk}/{tv}#s{s} L{L}"))
     return errs
 
 
@@ -300,7 +299,7 @@ def test_attn_equal_keys_give_mean(tq):
     vh = oracle.decode_rows(3, oracle.encode_rows(3, v, hkv, d), hkv, d).mean(axis=0)
     ref = np.repeat(vh, hq // hkv, axis=0)
     got = out.cpu().numpy()[0]
-    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < ATTN_TOL
+    assert_attn_close(got, ref, "decode equal keys")
 
 
 def test_attn_workspace_too_small_is_rejected(tq):
