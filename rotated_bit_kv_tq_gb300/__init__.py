@@ -20,8 +20,12 @@ __all__ = ["TQ_TURBO2", "TQ_TURBO3", "TQ_BLOCK_VALUES", "NOALLOC_SCRATCH_BYTES",
 
 def _stream_ptr(stream=None):
     import torch
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:   # the current stream's handle without building a Stream object
+        return ctypes.c_void_p(raw(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _ptr(t):

@@ -1,7 +1,10 @@
 // tq_api.cu -- the C ABI: host-side validation, codebook set-up, status word.
+#include <atomic>
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "tq_internal.cuh"
 
@@ -16,7 +19,17 @@ constexpr int kMaxDevices = 64;
 bool g_ready[kMaxDevices][2];
 Codebook g_host_cb[2];
 bool g_host_cb_done[2];
+std::atomic<float> g_h_scale[2];   // Codebook::h_scale, published once the table exists
 std::mutex g_mu;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+struct KernelState {
+    int smem = -1;      // dynamic shared-memory limit set so far
+    int threads = 0;    // occupancy computed for this block size and smem
+    int per_sm = 0;
+};
+std::map<std::pair<const void *, int>, KernelState> g_kernels;
+std::mutex g_kernels_mu;
 
 bool valid_type(int type) { return type == TQ_TURBO2 || type == TQ_TURBO3; }
 
@@ -80,6 +93,7 @@ const Codebook &host_codebook(int type) {
             cb.threshold[j] = (cb.centroid[j] + cb.centroid[j + 1]) * 0.5f;
         g_host_cb[i] = cb;
         g_host_cb_done[i] = true;
+        g_h_scale[i].store(cb.h_scale);
     }
     return g_host_cb[i];
 }
@@ -88,6 +102,8 @@ const Codebook &host_codebook(int type) {
 
 float centroid_h_scale(int type) {
     if (!valid_type(type)) return 1.0f;
+    const float h = g_h_scale[cb_index(type)].load();
+    if (h > 0.0f) return h;   // published by host_codebook (always, once a cache is valid)
     std::lock_guard<std::mutex> lock(g_mu);
     return host_codebook(type).h_scale;
 }
@@ -102,9 +118,37 @@ tq_status check_cuda(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_C
 int device_sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < kMaxDevices && (n = g_sm_count[dev].load()) > 0) return n;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         return 1;
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(n);
     return n;
+}
+
+tq_status kernel_setup(const void *kernel, int smem_bytes, int threads, int *per_sm) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_kernels_mu);
+    KernelState &st = g_kernels[std::make_pair(kernel, dev)];
+    if (st.smem < smem_bytes) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+            cudaSuccess)
+            return TQ_ERR_CUDA;
+        st.smem = smem_bytes;
+        st.threads = 0;
+    }
+    if (per_sm) {
+        if (st.threads != threads) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, st.smem) !=
+                cudaSuccess)
+                return TQ_ERR_CUDA;
+            st.threads = threads;
+            st.per_sm = n < 1 ? 1 : n;
+        }
+        *per_sm = st.per_sm;
+    }
+    return TQ_OK;
 }
 
 CacheView make_view(const tq_cache &c) {

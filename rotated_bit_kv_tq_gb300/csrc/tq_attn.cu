@@ -50,11 +50,17 @@ struct SplitPlan {
 
 SplitPlan plan_splits(int n_seqs, int head_dim, int64_t max_len, int sm_count) {
     SplitPlan pl;
-    // one wave of one CTA per SM, whatever the head size
     (void)head_dim;
-    const int64_t ctas = sm_count;
-    const int64_t target = max64(1, (ctas + n_seqs - 1) / n_seqs);
-    int64_t tps = (max64(max_len, 1) + target - 1) / target;
+    // One wave of one CTA per SM if every sequence had max_len tokens.  The host knows only
+    // the longest length: in a batch of mixed lengths the trailing splits of the shorter
+    // sequences are empty (those CTAs end at once), so long splits would leave a tail of a
+    // few long CTAs.  When a CTA would get more than kLongSplit tokens of a batch, the splits
+    // are cut to a quarter (at least kMinSplit tokens): several waves of short CTAs, which
+    // the scheduler balances.
+    constexpr int64_t kLongSplit = 2048, kMinSplit = 1024;
+    const int64_t per_seq = max64(1, (sm_count + n_seqs - 1) / n_seqs);
+    int64_t tps = (max64(max_len, 1) + per_seq - 1) / per_seq;
+    if (n_seqs > 1 && tps > kLongSplit) tps = max64(kMinSplit, (tps + 3) / 4);
     tps = (tps + kTokenAlign - 1) / kTokenAlign * kTokenAlign;
     if (tps < kTokenAlign) tps = kTokenAlign;
     pl.tokens_per_split = (int)tps;
@@ -407,9 +413,9 @@ template <int TK, int TV>
 tq_status launch_attn_t(const AttnParams &p, int n_seqs, cudaStream_t stream) {
     const size_t smem = partial_smem(p);
     if (smem > 220 * 1024) return TQ_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(attn_partial_kernel<TK, TV>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return TQ_ERR_CUDA;
+    const tq_status st = kernel_setup(reinterpret_cast<const void *>(attn_partial_kernel<TK, TV>),
+                                      (int)smem, kThreads, nullptr);
+    if (st != TQ_OK) return st;
     attn_partial_kernel<TK, TV><<<dim3(p.n_splits, n_seqs), kThreads, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return TQ_ERR_CUDA;
     return launch_merge(p, n_seqs, stream);

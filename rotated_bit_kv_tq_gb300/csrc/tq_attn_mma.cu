@@ -704,9 +704,11 @@ template <int TK, int TV, int NB, bool APPEND, bool QLO2>
 tq_status launch_tt(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     const size_t qbytes = q_bytes(p.n_q_heads, NB);
     const size_t smem = qbytes + 128 + (size_t)p.stages * p.stage_bytes;
-    if (cudaFuncSetAttribute(attn_mma_kernel<TK, TV, NB, APPEND, QLO2>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return TQ_ERR_CUDA;
+    // the most any shape asks for, so the attribute is set once per device
+    (void)smem;
+    const tq_status st = kernel_setup(reinterpret_cast<const void *>(attn_mma_kernel<TK, TV, NB, APPEND, QLO2>),
+                                      (int)kSmemBudget, 32 * consumers(NB), nullptr);
+    if (st != TQ_OK) return st;
     PdlConfig lc(dim3(p.n_splits, n_seqs), dim3(32 * consumers(NB)), smem, stream);
     lc.attrs[1].id = cudaLaunchAttributeClusterDimension;
     lc.attrs[1].val.clusterDim.x = kClusterSplits;

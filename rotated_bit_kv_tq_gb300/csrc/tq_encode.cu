@@ -330,14 +330,10 @@ template <int TYPE>
 tq_status launch_encode_t(const EncodeParams &p0, const EncodeParams &p1, int n_caches,
                           cudaStream_t stream) {
     const size_t smem = sizeof(EncodeSmem<TYPE>);
-    if (cudaFuncSetAttribute(encode_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-        return TQ_ERR_CUDA;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<TYPE>, kThreads,
-                                                      smem) != cudaSuccess)
-        return TQ_ERR_CUDA;
-    if (per_sm < 1) per_sm = 1;
+    const tq_status st = kernel_setup(reinterpret_cast<const void *>(encode_kernel<TYPE>),
+                                      (int)smem, kThreads, &per_sm);
+    if (st != TQ_OK) return st;
     const int64_t slots = max64(1, (int64_t)device_sm_count() * per_sm / n_caches);
     const int64_t grid = min64(max64(p0.n_tiles, p1.n_tiles), slots);
     PdlConfig lc(dim3((unsigned)grid, (unsigned)n_caches), dim3(kThreads), smem, stream);

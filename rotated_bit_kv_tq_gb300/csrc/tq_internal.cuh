@@ -151,7 +151,12 @@ __host__ __device__ constexpr int cb_index(int type) { return type == TQ_TURBO3 
 // ------------------------------------------------------------------ host side
 bool codebook_ready(int type, int device);
 tq_status check_cuda(cudaError_t e);
-int device_sm_count();
+int device_sm_count();   // SM count of the current device (queried once per device)
+// One-time set-up of a kernel on the current device, cached per (kernel, device): raises
+// its dynamic shared-memory limit to smem_bytes and computes how many CTAs of `threads`
+// threads and smem_bytes bytes fit on one SM (*per_sm, may be null).  Later calls with the
+// same or a smaller size cost a table lookup instead of two runtime calls.
+tq_status kernel_setup(const void *kernel, int smem_bytes, int threads, int *per_sm);
 CacheView make_view(const tq_cache &c);
 tq_status validate_cache(const tq_cache *c);
 // Argument checks of the single-token attention entry points (tq_attn_decode,

@@ -665,9 +665,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
 template <int TK, int TV>
 tq_status launch_tc_t(const TcParams &p, unsigned n_ctas, cudaStream_t stream) {
     const size_t smem = sizeof(TcSmem) + 1024;   // room to align the tiles to 1024 bytes
-    if (cudaFuncSetAttribute(prefill_tc_kernel<TK, TV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-        return TQ_ERR_CUDA;
+    const tq_status st = kernel_setup(reinterpret_cast<const void *>(prefill_tc_kernel<TK, TV>),
+                                      (int)smem, kTcThreads, nullptr);
+    if (st != TQ_OK) return st;
     PdlConfig lc(dim3(n_ctas), dim3(kTcThreads), smem, stream);
     return check_cuda(cudaLaunchKernelEx(&lc.cfg, prefill_tc_kernel<TK, TV>, p));
 }
