@@ -59,12 +59,13 @@ constexpr size_t kSmemBudget = 227 * 1024;   // per CTA (one per SM): the sm_100
 
 // Rotated queries in shared memory, in MMA-fragment order: head h, block b, k-step j and
 // lane quarter q4 hold the four values 32 q4 + 4j .. +3 at halfs h*QS + 128 b + 16 j + 4 q4
-// (the high fp16 parts; the low parts follow in the same layout, Hq * QS halfs later).
+// (the high fp16 parts; the low parts follow in the same layout, Hq * QS halfs later, then
+// one row of zeros that lanes without a head read, so their loads need no select).
 // QS = 128 nb + 16 puts consecutive heads 8 banks apart, so each half-warp's 8-byte
 // B-fragment loads (four heads x four quarters) cover all 32 banks once.
 __host__ __device__ constexpr int q_stride(int nb) { return 128 * nb + 16; }
 inline size_t q_bytes(int n_q_heads, int nb) {
-    return ((size_t)2 * n_q_heads * q_stride(nb) * 2 + 127) & ~size_t(127);
+    return ((size_t)(2 * n_q_heads + 1) * q_stride(nb) * 2 + 127) & ~size_t(127);
 }
 
 struct MmaParams {
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
 
     constexpr int QS = q_stride(NB);
     __half *qh = reinterpret_cast<__half *>(smem);                          // [Hq][QS]
-    const size_t qbytes = ((size_t)2 * Hq * QS * 2 + 127) & ~size_t(127);
+    const size_t qbytes = ((size_t)(2 * Hq + 1) * QS * 2 + 127) & ~size_t(127);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + qbytes);          // [stages]
     uint64_t *empty = full + 4;                                            // [stages]
     uint8_t *stage0 = smem + qbytes + 128;
@@ -225,10 +226,8 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     uint2 enc_raw = make_uint2(0u, 0u);   // this warp's first block, loaded with the query
     if (owner && warp < 2 * bpr) enc_raw = warp_block_load(enc_src(warp), lane);
     // Thread 0 requests the first tile as soon as the sequence length is known and the rest
-    // of the ring after the rotation; warps 1-15 rotate the query meanwhile, so the query
-    // loads and the length load are in flight together (measured at 32K context: 23.2 us
-    // per call, against 24.4 with warp 0 rotating too and 25.6 with every stage requested
-    // after the rotation).
+    // of the ring once that tile has landed; warps 1-15 rotate the query meanwhile, so the
+    // query loads and the length load are in flight together.
     auto issue = [&](int i) {
         if (p.withhold_tiles) return;   // injected fault: nothing is copied, no copy in flight
         const int64_t t0 = tile_start(i);
@@ -237,6 +236,9 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i % p.stages]));
     };
     if (tid == 0 && n_tiles > 0) issue(0);
+    if (warp == 0)   // the zero row of lanes without a head (warp 0 rotates nothing)
+        for (int i = lane; i < QS / 8; i += 32)
+            reinterpret_cast<uint4 *>(qh + 2 * Hq * QS)[i] = make_uint4(0u, 0u, 0u, 0u);
     // ---- rotate q once per call: y = W q_b * score_scale, stored as hi = fp16(y) and
     // lo = fp16(y - hi), by warps 1-15; a warp loads its (up to five) query blocks at once,
     // then rotates them
@@ -271,8 +273,6 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             *reinterpret_cast<uint2 *>(dst + Hq * QS) = lo;
         }
     }
-    if (tid == 0)   // no copy in this loop reads the new row (see above)
-        for (int i = 1; i < n_tiles && i < p.stages; ++i) issue(i);
     if (owner) {
         // the new row's slot in its stage (used when new_in_stage)
         uint8_t *sk = stage0 + (size_t)(i_new % p.stages) * p.stage_bytes;
@@ -324,16 +324,15 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         // QLO2, column n < 4 holds the high part of head n and column 4 + n its low part;
         // with QLO2, column n holds head n, high part in the first MMA, low in the second.
         const int qhead = QLO2 ? g8 : (g8 & 3);
-        const bool qv = qhead < G;
-        const __half *qrow = qh + ((QLO2 || g8 < 4 ? 0 : Hq) + g * G + (qv ? qhead : 0)) * QS + 4 * q4;
-        const __half *qrow_lo = qrow + Hq * QS;
+        const __half *qrow = qhead < G
+            ? qh + ((QLO2 || g8 < 4 ? 0 : Hq) + g * G + qhead) * QS + 4 * q4
+            : qh + 2 * Hq * QS + 4 * q4;                                  // the zero row
+        const __half *qrow_lo = qhead < G ? qrow + Hq * QS : qrow;
         auto bq = [&](int b, int j) -> uint2 {
-            const uint2 v = *reinterpret_cast<const uint2 *>(qrow + b * kBlock + 16 * j);
-            return qv ? v : make_uint2(0u, 0u);
+            return *reinterpret_cast<const uint2 *>(qrow + b * kBlock + 16 * j);
         };
         auto bq_lo = [&](int b, int j) -> uint2 {
-            const uint2 v = *reinterpret_cast<const uint2 *>(qrow_lo + b * kBlock + 16 * j);
-            return qv ? v : make_uint2(0u, 0u);
+            return *reinterpret_cast<const uint2 *>(qrow_lo + b * kBlock + 16 * j);
         };
         HalfTables tk, tv;
         {
@@ -375,6 +374,11 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                 timed_out = true;
                 break;
             }
+            // the rest of the ring once the first tile has landed, so that the first tiles of
+            // all CTAs do not share the HBM with the second ones (no copy of these reads the
+            // new row: see above)
+            if (i == 0 && tid == 0)
+                for (int k = 1; k < n_tiles && k < p.stages; ++k) issue(k);
             const int nt = tile_len(i);
             const uint8_t *Kt = stage0 + (size_t)s * p.stage_bytes;
             const uint8_t *Vt = Kt + (size_t)TT * Rk;
@@ -402,11 +406,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     const int rA = hr0 + 16 * mt + g8, rB = rA + 8;
-                    float acc[2][4];
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+                    float acc[2][4];   // the first k-step of each block writes it (zero C)
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
@@ -421,8 +421,13 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                                 group_pairs<TK>(qb, ww, r, tk, ks, xb);
                                 const int j = 4 * ww + 2 * r;
                                 const uint2 q0 = bq(b, j), q1 = bq(b, j + 1);
-                                mma16816(acc[0], xa[0], xb[0], xa[1], xb[1], q0.x, q0.y);
-                                mma16816(acc[1], xa[2], xb[2], xa[3], xb[3], q1.x, q1.y);
+                                if (ww == 0 && r == 0) {
+                                    mma16816_z(acc[0], xa[0], xb[0], xa[1], xb[1], q0.x, q0.y);
+                                    mma16816_z(acc[1], xa[2], xb[2], xa[3], xb[3], q1.x, q1.y);
+                                } else {
+                                    mma16816(acc[0], xa[0], xb[0], xa[1], xb[1], q0.x, q0.y);
+                                    mma16816(acc[1], xa[2], xb[2], xa[3], xb[3], q1.x, q1.y);
+                                }
                                 if (QLO2) {
                                     const uint2 l0 = bq_lo(b, j), l1 = bq_lo(b, j + 1);
                                     mma16816(acc[0], xa[0], xb[0], xa[1], xb[1], l0.x, l0.y);
@@ -434,10 +439,6 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                         s1 = fmaf(nA, acc[0][1] + acc[1][1], s1);
                         s2 = fmaf(nB, acc[0][2] + acc[1][2], s2);
                         s3 = fmaf(nB, acc[0][3] + acc[1][3], s3);
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
                     }
                     if (!QLO2) {   // add the low parts' columns 4 + n (lane q4 ^ 2)
                         s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
