@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTokenAlign = 16;       // split ranges start on multiples of this
+constexpr int kMinSplitTokens = 16;       // fewest tokens per split
 constexpr int kMaxG = 8;              // query heads per KV head handled in registers
 constexpr int kMaxNb = 2;             // 128-blocks per head handled in registers
 constexpr int kTileBudget = 96 * 1024;  // shared bytes for one K+V tile
@@ -61,8 +61,10 @@ SplitPlan plan_splits(int n_seqs, int head_dim, int64_t max_len, int sm_count) {
     const int64_t per_seq = max64(1, (sm_count + n_seqs - 1) / n_seqs);
     int64_t tps = (max64(max_len, 1) + per_seq - 1) / per_seq;
     if (n_seqs > 1 && tps > kLongSplit) tps = max64(kMinSplit, (tps + 3) / 4);
-    tps = (tps + kTokenAlign - 1) / kTokenAlign * kTokenAlign;
-    if (tps < kTokenAlign) tps = kTokenAlign;
+    // no rounding of tps: a split may start at any row (tiles and page runs do not care),
+    // and rounding up would leave SMs idle (32,896 tokens: 148 CTAs of 224 instead of 152
+    // of 217)
+    if (tps < kMinSplitTokens) tps = kMinSplitTokens;
     pl.tokens_per_split = (int)tps;
     pl.n_splits = (int)max64(1, (max_len + tps - 1) / tps);
     // whole clusters of splits (trailing splits with no tokens write neutral partials)
