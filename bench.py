@@ -76,6 +76,9 @@ def parse():
     ap.add_argument("--kernel-probe", type=int, default=0, metavar="CTX",
                     help="time one layer's encode and attention at context CTX (the small "
                          "case the ncu captures use) instead of the full benchmark")
+    ap.add_argument("--phase-trace", type=int, default=0, metavar="CTX",
+                    help="per-phase globaltimer trace of the decode step (traced library, "
+                         "32 layers of the workload's shape at context CTX, graph replay)")
     ap.add_argument("--prefill-probe", type=int, default=0, metavar="CTX",
                     help="time one layer's prompt attention over a whole CTX-token prompt "
                          "(one chunk from position 0; the small case of the prefill capture)")
@@ -740,6 +743,85 @@ def kernel_probe(args):
                       "status": tq.device_status()}))
 
 
+TRACE_PHASES = {
+    "attention": ["entry", "dependency wait returned", "sequence length loaded",
+                  "first tile requested", "query rotated (CTA barrier)", "first tile landed",
+                  "loop end (slowest warp)", "epilogue done (cluster barrier)",
+                  "cluster merge done"],
+    "merge": ["entry", "dependency wait returned", "partial rows loaded", "output stored"],
+}
+
+
+def phase_trace(args):
+    """Decode step of every layer of the workload's shape at context CTX, replayed from a
+    CUDA graph through the traced library (rotated_bit_kv_tq_gb300.build(trace=True)); prints
+    the per-layer call time and, for the last layer's call, each phase's time across CTAs
+    (min / median / max, us after the first CTA's dependency wait returned)."""
+    import ctypes
+    import torch
+    from rotated_bit_kv_tq_gb300 import _lib, build
+    lib = _lib.load(build.build(trace=True))     # the traced library, before any other load
+    import rotated_bit_kv_tq_gb300 as tq
+    lib.tq_phase_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    w = workload(args.workload)
+    tt = w.types[0]
+    tq.codebook_init(tt, 0)
+    L, Hkv, Hq, D, T = w.layers, w.n_kv_heads, w.n_q_heads, w.head_dim, args.phase_trace
+    max_len = T + 1
+    k16 = torch.from_numpy(synth.kv_tokens(w, 0, "K", 0, max_len).reshape(max_len, -1)).cuda()
+    v16 = torch.from_numpy(synth.kv_tokens(w, 0, "V", 0, max_len).reshape(max_len, -1)).cuda()
+    kc = [tq.KVCache(tt, Hkv, D, capacity_tokens=max_len) for _ in range(L)]
+    vc = [tq.KVCache(tt, Hkv, D, capacity_tokens=max_len) for _ in range(L)]
+    for l in range(L):   # prompt rows of every layer from layer 0's draws (timing only)
+        tq.encode_kv(kc[l], vc[l], k16[:T], v16[:T])
+    q = torch.from_numpy(np.stack([synth.query(w, l, 0) for l in range(L)])).cuda().reshape(L, 1, Hq, D)
+    kn, vn = k16[T:].reshape(1, Hkv, D), v16[T:].reshape(1, Hkv, D)
+    out = torch.empty(L, 1, Hq, D, device="cuda")
+    ws = torch.empty(tq.attn_workspace_bytes(1, Hq, D, max_len), dtype=torch.uint8, device="cuda")
+    lens = torch.tensor([max_len], dtype=torch.int32, device="cuda")
+
+    def iteration():
+        for l in range(L):
+            tq.attn_decode_append(kc[l], vc[l], kn, vn, q[l], lens, max_len, out[l], ws)
+
+    iteration()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+        iteration()
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    call_us = e0.elapsed_time(e1) / (10 * L) * 1e3
+    assert lib.tq_phase_trace_clear() == 0
+    g.replay()
+    torch.cuda.synchronize()
+    n_slots, n_points = 4096, 12
+    tr = np.zeros((n_slots, n_points), np.uint64)
+    assert lib.tq_phase_trace_read(tr.ctypes.data, tr.nbytes) == 0
+    att, mrg = tr[:2048].astype(np.int64), tr[2048:].astype(np.int64)
+    att, mrg = att[att[:, 1] > 0], mrg[mrg[:, 1] > 0]
+    t0 = att[:, 1].min()
+    res = {"probe": f"{w.name} decode-step phases", "ctx": max_len, "layers": L,
+           "call_us": call_us, "attention_ctas": int(len(att)), "merge_ctas": int(len(mrg)),
+           "phases_us": {}}
+    for kind, arr in (("attention", att), ("merge", mrg)):
+        for i, name in enumerate(TRACE_PHASES[kind]):
+            col = (arr[:, i][arr[:, i] > 0] - t0) / 1e3
+            if len(col):
+                res["phases_us"][f"{kind}: {name}"] = [round(float(col.min()), 2),
+                                                       round(float(np.median(col)), 2),
+                                                       round(float(col.max()), 2)]
+    print(json.dumps(res, indent=1))
+
+
 def prefill_probe(args):
     """One layer of the workload's shape: encode a CTX-token prompt's K and V, then run the
     whole prompt as one causal chunk; per-call times from CUDA events (not a bench line)."""
@@ -780,6 +862,9 @@ def main():
         return
     if args.prefill_probe:
         prefill_probe(args)
+        return
+    if args.phase_trace:
+        phase_trace(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

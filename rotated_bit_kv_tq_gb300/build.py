@@ -40,24 +40,32 @@ def _deps():
     return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "tq.h")]
 
 
-def _up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# The traced library (phase stamps of the decode-attention kernels, TQ_TRACE_PHASES), for
+# bench.py --phase-trace; never loaded by the product path.
+TRACE_BUILD = os.path.join(HERE, "_build_trace")
+TRACE_LIB = os.path.join(HERE, "libtq_trace.so")
+
+
+def _up_to_date(lib) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not ptxas_info and _up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          trace: bool = False) -> str:
+    out_lib, out_dir = (TRACE_LIB, TRACE_BUILD) if trace else (LIB, BUILD)
+    if not force and not ptxas_info and _up_to_date(out_lib):
+        return out_lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     objs = []
     jobs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *NVFLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *NVFLAGS, *(["-DTQ_TRACE_PHASES"] if trace else []), "-c", src, "-o", obj]
         if src.endswith(".cpp"):
             cmd[1:1] = ["-x", "cu"]
         if ptxas_info:
@@ -74,16 +82,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                 sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             if r.returncode:
                 raise RuntimeError(f"nvcc failed on {cmd[-3]}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out_lib + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-rdc=true", *objs, "-o", tmp]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode:
         sys.stderr.write(" ".join(link) + "\n" + r.stdout + r.stderr)
         raise RuntimeError("nvcc link of libtq.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv, ptxas_info="--ptxas" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                ptxas_info="--ptxas" in sys.argv, trace="--trace" in sys.argv))

@@ -11,6 +11,9 @@
 namespace tq {
 
 __device__ int32_t g_status = 0;
+#if defined(TQ_TRACE_PHASES)
+__device__ unsigned long long g_phase_trace[2 * kTraceCtas][kTracePoints];
+#endif
 __constant__ Codebook c_codebook[2];
 
 namespace {
@@ -395,6 +398,19 @@ tq_status tq_device_status(void *stream, int32_t *status_out) {
     *status_out = host;
     return TQ_OK;
 }
+
+#if defined(TQ_TRACE_PHASES)
+// Traced library only: copy the phase stamps (2 * kTraceCtas x kTracePoints u64) to host
+// memory, or clear them.  Not part of the product ABI.
+TQ_API int tq_phase_trace_read(void *host, size_t bytes) {
+    return (int)cudaMemcpyFromSymbol(host, g_phase_trace, bytes);
+}
+TQ_API int tq_phase_trace_clear(void) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_phase_trace) != cudaSuccess) return 1;
+    return (int)cudaMemset(p, 0, sizeof g_phase_trace);
+}
+#endif
 
 const char *tq_status_str(int status) {
     switch (status) {

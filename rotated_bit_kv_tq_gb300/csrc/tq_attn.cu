@@ -318,9 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
 constexpr int kMergeRows = 24;
 
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
+    const int trace_slot = kTraceCtas + blockIdx.y * gridDim.x + blockIdx.x;   // phase trace only
+    (void)trace_slot;
+    if (threadIdx.x == 0) TQ_PHASE(trace_slot, 0);
     // launched as a programmatic dependent of the partial kernel: wait for its results
     pdl_wait();
     pdl_launch_dependents();
+    if (threadIdx.x == 0) TQ_PHASE(trace_slot, 1);
     __shared__ float red_m[8], red_l[8];
     __shared__ float4 red_o[8][32];
     const int h = blockIdx.x, seq = blockIdx.y, b = blockIdx.z, D = p.head_dim;
@@ -369,6 +373,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
         }
     }
     red_o[warp][lane] = acc;
+    if (threadIdx.x == 0 && acc.x != acc.x + 1.0f) TQ_PHASE(trace_slot, 2);   // loads consumed
     if (lane == 0) {
         red_m[warp] = M;
         red_l[warp] = lsum;
@@ -397,6 +402,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     apply_signs4(v, p.vc, 4 * lane);     // inverse D W of the V cache
     float4 o4 = make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
     *reinterpret_cast<float4 *>(p.out + ((int64_t)seq * p.n_q_heads + h) * D + b * kBlock + 4 * lane) = o4;
+    if (lane == 0) TQ_PHASE(trace_slot, 3);
 }
 
 size_t partial_smem(const AttnParams &p) {

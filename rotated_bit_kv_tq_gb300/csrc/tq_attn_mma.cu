@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     const int Rk = p.kc.row_bytes, Rv = p.vc.row_bytes;
     const int TT = p.tile_tokens;
     const int seq = blockIdx.y, split = blockIdx.x;
+    const int trace_slot = blockIdx.y * gridDim.x + blockIdx.x;   // phase trace only
+    (void)trace_slot;
+    if (tid == 0) TQ_PHASE(trace_slot, 0);
 
     constexpr int QS = q_stride(NB);
     __half *qh = reinterpret_cast<__half *>(smem);                          // [Hq][QS]
@@ -220,12 +223,14 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     // the kernel launched before this one
     pdl_wait();
     pdl_launch_dependents();
+    if (tid == 0) TQ_PHASE(trace_slot, 1);
 
     int64_t len = p.seq_lens[seq];
     if (len < 0 || len > p.max_len) {
         if (tid == 0) record_error(TQ_ERR_OUT_OF_RANGE);
         len = len < 0 ? 0 : p.max_len;
     }
+    if (tid == 0) TQ_PHASE(trace_slot, 2);
     const int64_t t_begin = (int64_t)split * p.tokens_per_split;
     const int64_t t_end = min64(len, t_begin + p.tokens_per_split);
     // Tile 0 holds TT / 2 tokens, the others TT: with every CTA requesting its first tile
@@ -264,6 +269,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i % p.stages]));
     };
     if (tid == 0 && n_tiles > 0) issue(0);
+    if (tid == 0) TQ_PHASE(trace_slot, 3);
     if (warp == 0)   // the zero row of lanes without a head (warp 0 rotates nothing)
         for (int i = lane; i < QS / 8; i += 32)
             reinterpret_cast<uint4 *>(qh + 2 * Hq * QS)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -331,6 +337,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         if (!new_in_stage) asm volatile("fence.proxy.async.global;\n" ::: "memory");
     }
     __syncthreads();
+    if (tid == 0) TQ_PHASE(trace_slot, 4);
 
     bool timed_out = false;
 
@@ -405,6 +412,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             // the rest of the ring once the first tile has landed, so that the first tiles of
             // all CTAs do not share the HBM with the second ones (no copy of these reads the
             // new row: see above)
+            if (i == 0 && tid == 0) TQ_PHASE(trace_slot, 5);
             if (i == 0 && tid == 0)
                 for (int k = 1; k < n_tiles && k < p.stages; ++k) issue(k);
             const int nt = tile_len(i);
@@ -578,6 +586,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         }
     }
 
+    if (lane == 0) TQ_PHASE_MAX(trace_slot, 6);
     // ---------------- epilogue: combine the lanes' sums, the warps of one KV head, write
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -661,6 +670,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     // ---------------- the CTAs of a cluster (consecutive splits) merge their partials
     // through distributed shared memory: CTA rank r owns heads r, r + CL, ...
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+    if (tid == 0) TQ_PHASE(trace_slot, 7);
     {
         uint32_t rank;
         asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
@@ -725,6 +735,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             }
         }
     }
+    if (tid == 0) TQ_PHASE(trace_slot, 8);
     // nobody leaves while a peer may still read its shared memory
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }

@@ -111,6 +111,28 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ phase trace
+// Only in the traced library (TQ_TRACE_PHASES; build.build(trace=True) makes libtq_trace.so):
+// %globaltimer stamps at phase boundaries of every CTA of the decode-attention and merge
+// kernels, read back through tq_phase_trace_read.  The product library has no trace code.
+constexpr int kTraceCtas = 2048;     // attention CTA slots; merge CTAs at kTraceCtas + index
+constexpr int kTracePoints = 12;
+#if defined(TQ_TRACE_PHASES)
+extern __device__ unsigned long long g_phase_trace[2 * kTraceCtas][kTracePoints];
+__device__ __forceinline__ unsigned long long phase_clock() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+#define TQ_PHASE(slot, point) \
+    do { if ((slot) < 2 * kTraceCtas) g_phase_trace[(slot)][(point)] = phase_clock(); } while (0)
+#define TQ_PHASE_MAX(slot, point) \
+    do { if ((slot) < 2 * kTraceCtas) atomicMax(&g_phase_trace[(slot)][(point)], phase_clock()); } while (0)
+#else
+#define TQ_PHASE(slot, point) ((void)0)
+#define TQ_PHASE_MAX(slot, point) ((void)0)
+#endif
+
 // Launch configuration with the programmatic-serialization attribute set (attrs[0]); a
 // caller may add a second attribute at attrs[1].
 struct PdlConfig {
