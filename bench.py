@@ -766,19 +766,37 @@ def phase_trace(args):
     w = workload(args.workload)
     tt = w.types[0]
     tq.codebook_init(tt, 0)
-    L, Hkv, Hq, D, T = w.layers, w.n_kv_heads, w.n_q_heads, w.head_dim, args.phase_trace
-    max_len = T + 1
-    k16 = torch.from_numpy(synth.kv_tokens(w, 0, "K", 0, max_len).reshape(max_len, -1)).cuda()
-    v16 = torch.from_numpy(synth.kv_tokens(w, 0, "V", 0, max_len).reshape(max_len, -1)).cuda()
-    kc = [tq.KVCache(tt, Hkv, D, capacity_tokens=max_len) for _ in range(L)]
-    vc = [tq.KVCache(tt, Hkv, D, capacity_tokens=max_len) for _ in range(L)]
-    for l in range(L):   # prompt rows of every layer from layer 0's draws (timing only)
-        tq.encode_kv(kc[l], vc[l], k16[:T], v16[:T])
-    q = torch.from_numpy(np.stack([synth.query(w, l, 0) for l in range(L)])).cuda().reshape(L, 1, Hq, D)
-    kn, vn = k16[T:].reshape(1, Hkv, D), v16[T:].reshape(1, Hkv, D)
-    out = torch.empty(L, 1, Hq, D, device="cuda")
-    ws = torch.empty(tq.attn_workspace_bytes(1, Hq, D, max_len), dtype=torch.uint8, device="cuda")
-    lens = torch.tensor([max_len], dtype=torch.int32, device="cuda")
+    L, Hkv, Hq, D, n = w.layers, w.n_kv_heads, w.n_q_heads, w.head_dim, w.n_seqs
+    row = Hkv * D
+    if n == 1:   # one sequence of CTX tokens plus the appended one
+        lens0 = np.array([args.phase_trace], np.int64)
+    else:        # the batched workload's drawn lengths (CTX is ignored)
+        lens0 = synth.seq_lens(w).astype(np.int64)
+    max_len = int(lens0.max()) + 1
+    # prompt rows of every layer from layer 0's draws (timing only), then the new token
+    ks = [synth.kv_tokens(w, 0, "K", 0, int(L0) + 1, s).reshape(int(L0) + 1, row) for s, L0 in enumerate(lens0)]
+    vs = [synth.kv_tokens(w, 0, "V", 0, int(L0) + 1, s).reshape(int(L0) + 1, row) for s, L0 in enumerate(lens0)]
+    if n == 1:
+        mk = lambda: tq.KVCache(tt, Hkv, D, capacity_tokens=max_len)  # noqa: E731
+    else:
+        pt, n_pages = synth.page_table(w, max_len)
+        ptd = torch.from_numpy(pt).cuda()
+        mk = lambda: tq.KVCache(tt, Hkv, D, n_seqs=n, page_tokens=w.page_tokens, page_table=ptd,  # noqa: E731
+                                n_pages=n_pages)
+    kc = [mk() for _ in range(L)]
+    vc = [mk() for _ in range(L)]
+    for s in range(n):
+        kd = torch.from_numpy(ks[s][:-1]).cuda()
+        vd = torch.from_numpy(vs[s][:-1]).cuda()
+        for l in range(L):
+            tq.encode_kv(kc[l], vc[l], kd, vd, seq_id=s)
+    q = torch.from_numpy(np.stack([np.stack([synth.query(w, l, 0, s) for s in range(n)])
+                                   for l in range(L)])).cuda()
+    kn = torch.from_numpy(np.stack([k[-1] for k in ks])).cuda().reshape(n, Hkv, D)
+    vn = torch.from_numpy(np.stack([v[-1] for v in vs])).cuda().reshape(n, Hkv, D)
+    out = torch.empty(L, n, Hq, D, device="cuda")
+    ws = torch.empty(tq.attn_workspace_bytes(n, Hq, D, max_len), dtype=torch.uint8, device="cuda")
+    lens = torch.from_numpy((lens0 + 1).astype(np.int32)).cuda()
 
     def iteration():
         for l in range(L):
@@ -809,7 +827,11 @@ def phase_trace(args):
     att, mrg = tr[:2048].astype(np.int64), tr[2048:].astype(np.int64)
     att, mrg = att[att[:, 1] > 0], mrg[mrg[:, 1] > 0]
     t0 = att[:, 1].min()
-    res = {"probe": f"{w.name} decode-step phases", "ctx": max_len, "layers": L,
+    busy = (att[:, 8] - att[:, 1]) / 1e3     # dependency wait to cluster merge done, per CTA
+    res = {"probe": f"{w.name} decode-step phases", "ctx": max_len, "layers": L, "n_seqs": n,
+           "cta_busy_us": {"sum_over_ctas": round(float(busy.sum()), 1),
+                           "sum_with_tiles": round(float(busy[att[:, 5] > 0].sum()), 1),
+                           "ctas_with_tiles": int((att[:, 5] > 0).sum())},
            "call_us": call_us, "attention_ctas": int(len(att)), "merge_ctas": int(len(mrg)),
            "phases_us": {}}
     for kind, arr in (("attention", att), ("merge", mrg)):

@@ -67,8 +67,10 @@ SplitPlan plan_splits(int n_seqs, int head_dim, int64_t max_len, int sm_count) {
     if (tps < kMinSplitTokens) tps = kMinSplitTokens;
     pl.tokens_per_split = (int)tps;
     pl.n_splits = (int)max64(1, (max_len + tps - 1) / tps);
-    // whole clusters of splits (trailing splits with no tokens write neutral partials)
-    pl.n_splits = (pl.n_splits + kClusterSplits - 1) / kClusterSplits * kClusterSplits;
+    // one sequence: whole clusters of splits (a trailing split with no tokens writes neutral
+    // partials); a batch runs without clusters
+    if (n_seqs == 1)
+        pl.n_splits = (pl.n_splits + kClusterSplits - 1) / kClusterSplits * kClusterSplits;
     return pl;
 }
 
@@ -405,6 +407,53 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     if (lane == 0) TQ_PHASE(trace_slot, 3);
 }
 
+// Few partial rows per head (batches): one warp merges one (head, sequence, block).  Lane r
+// loads the (m, l) of row r and every lane the float4 of its coordinates of every row, all in
+// one round; the warp reduces with shuffles and applies the inverse FWHT itself.
+constexpr int kMergeWarpRows = 16;   // rows one warp merges in its single round of loads
+
+__global__ void __launch_bounds__(256) attn_merge_warp_kernel(const AttnParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);   // (head, block) of sequence blockIdx.y
+    const int D = p.head_dim, Hq = p.n_q_heads;
+    if (item >= Hq * p.nb) return;
+    const int b = item % p.nb, h = item / p.nb;
+    const int64_t seq = blockIdx.y;
+    const int R = p.n_splits;
+    const float *base = p.part + (seq * R * Hq + h) * part_stride(D);
+    const int64_t sstride = (int64_t)Hq * part_stride(D);
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < R) ml = *reinterpret_cast<const float2 *>(base + lane * sstride + D);
+    float4 v[kMergeWarpRows];
+#pragma unroll
+    for (int r = 0; r < kMergeWarpRows; ++r)
+        v[r] = r < R ? *reinterpret_cast<const float4 *>(base + r * sstride + b * kBlock + 4 * lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = ml.x == -INFINITY ? 0.f : __expf(ml.x - M);
+    float L = w * ml.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    float o4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kMergeWarpRows; ++r) {
+        const float wr = __shfl_sync(0xffffffffu, w, r);
+        o4[0] = fmaf(wr, v[r].x, o4[0]);
+        o4[1] = fmaf(wr, v[r].y, o4[1]);
+        o4[2] = fmaf(wr, v[r].z, o4[2]);
+        o4[3] = fmaf(wr, v[r].w, o4[3]);
+    }
+    const float inv = L > 0.f ? kInvSqrt128 / L : 0.f;
+    warp_fwht4(o4, lane);                    // inverse rotation (1/sqrt(128)) W o_b
+    apply_signs4(o4, p.vc, 4 * lane);        // inverse D W of the V cache
+    *reinterpret_cast<float4 *>(p.out + (seq * Hq + h) * D + b * kBlock + 4 * lane) =
+        make_float4(o4[0] * inv, o4[1] * inv, o4[2] * inv, o4[3] * inv);
+}
+
 size_t partial_smem(const AttnParams &p) {
     const int Rk16 = (p.kc.row_bytes + 15) & ~15, Rv16 = (p.vc.row_bytes + 15) & ~15;
     return sizeof(float) * ((size_t)p.n_q_heads * p.head_dim + (size_t)p.n_q_heads * p.tile_tokens +
@@ -413,6 +462,11 @@ size_t partial_smem(const AttnParams &p) {
 }
 
 tq_status launch_merge(const AttnParams &p, int n_seqs, cudaStream_t stream) {
+    if (p.n_splits <= kMergeWarpRows) {   // one warp per (head, sequence, block)
+        PdlConfig lc(dim3((unsigned)((p.n_q_heads * p.nb + 7) / 8), (unsigned)n_seqs), dim3(256), 0,
+                     stream);
+        return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_merge_warp_kernel, p));
+    }
     PdlConfig lc(dim3(p.n_q_heads, n_seqs, p.nb), dim3(256), 0, stream);
     return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_merge_kernel, p));
 }
@@ -465,12 +519,13 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
                                         device_sm_count()))
         return TQ_ERR_WORKSPACE_TOO_SMALL;
     if (attn_mma_supported(k, v, n_q_heads)) {
+        const int cluster = n_seqs == 1 ? kClusterSplits : 1;
         tq_status st = launch_attn_mma(k, v, q, n_seqs, n_q_heads, seq_lens, max_seq_len, scale,
-                                       p.part, p.n_splits, p.tokens_per_split, k_new, v_new,
-                                       stream);
+                                       p.part, p.n_splits, p.tokens_per_split, cluster, k_new,
+                                       v_new, stream);
         if (st != TQ_OK) return st;
         AttnParams pm = p;
-        pm.n_splits = p.n_splits / kClusterSplits;   // one partial row per cluster
+        pm.n_splits = p.n_splits / cluster;   // one partial row per cluster
         return launch_merge(pm, n_seqs, stream);
     }
     if (p.group > kMaxG || p.nb > kMaxNb) return TQ_ERR_UNSUPPORTED;

@@ -84,6 +84,7 @@ struct MmaParams {
     int32_t stages;
     int32_t stage_bytes;
     int32_t cpart_offset;   // bytes from the first stage to this CTA's partial rows
+    int32_t cl;             // CTAs per cluster: 2 (pairs of splits merge in shared memory) or 1
     uint32_t wait_limit;    // polls per bounded mbarrier wait
     int32_t withhold_tiles; // fault injection: request no tile copies (every tile wait runs out)
     // 2, 4, 2^16, 2^30, 2^31: shift amounts as multipliers passed at run time, so that the
@@ -668,13 +669,15 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         }
     }
     // ---------------- the CTAs of a cluster (consecutive splits) merge their partials
-    // through distributed shared memory: CTA rank r owns heads r, r + CL, ...
+    // through distributed shared memory: CTA rank r owns heads r, r + CL, ...  (a cluster of
+    // one CTA writes its own partial rows)
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
     if (tid == 0) TQ_PHASE(trace_slot, 7);
     {
         uint32_t rank;
         asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-        constexpr int CL = kClusterSplits;
+        constexpr int CLM = kClusterSplits;   // the most CTAs a cluster has
+        const int CL = p.cl;
         const uint32_t local = smem_u32(cpart);
         const int group = split / CL;
         const int n_groups = p.n_splits / CL;
@@ -682,13 +685,14 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         // before using any
         constexpr int HW = 2;
         for (int h0 = (int)rank + CL * warp; h0 < Hq; h0 += HW * CL * kConsumers) {
-            float mc[HW][CL], lc[HW][CL];
-            float4 v[HW][CL][NB];
+            float mc[HW][CLM], lc[HW][CLM];
+            float4 v[HW][CLM][NB];
 #pragma unroll
             for (int k = 0; k < HW; ++k) {
                 const int h = min(h0 + k * CL * kConsumers, Hq - 1);
 #pragma unroll
-                for (int c = 0; c < CL; ++c) {
+                for (int c = 0; c < CLM; ++c) {
+                    if (c >= CL) break;
                     uint32_t ra;
                     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                                  : "=r"(ra) : "r"(local + (uint32_t)(h * PS + D) * 4u), "r"(c));
@@ -707,11 +711,16 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             for (int k = 0; k < HW; ++k) {
                 const int h = h0 + k * CL * kConsumers;
                 if (h >= Hq) break;
-                float M = -INFINITY, L = 0.f, wgt[CL];
+                float M = -INFINITY, L = 0.f, wgt[CLM];
 #pragma unroll
-                for (int c = 0; c < CL; ++c) M = fmaxf(M, mc[k][c]);
+                for (int c = 0; c < CLM; ++c)
+                    if (c < CL) M = fmaxf(M, mc[k][c]);
 #pragma unroll
-                for (int c = 0; c < CL; ++c) {
+                for (int c = 0; c < CLM; ++c) {
+                    if (c >= CL) {
+                        wgt[c] = 0.f;
+                        continue;
+                    }
                     wgt[c] = mc[k][c] == -INFINITY ? 0.f : __expf(mc[k][c] - M);
                     L += wgt[c] * lc[k][c];
                 }
@@ -720,7 +729,8 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                 for (int b = 0; b < NB; ++b) {
                     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int c = 0; c < CL; ++c) {
+                    for (int c = 0; c < CLM; ++c) {
+                        if (c >= CL) break;
                         a.x = fmaf(wgt[c], v[k][c][b].x, a.x);
                         a.y = fmaf(wgt[c], v[k][c][b].y, a.y);
                         a.z = fmaf(wgt[c], v[k][c][b].z, a.z);
@@ -751,7 +761,7 @@ tq_status launch_tt(const MmaParams &p, int n_seqs, cudaStream_t stream) {
     if (st != TQ_OK) return st;
     PdlConfig lc(dim3(p.n_splits, n_seqs), dim3(32 * consumers(NB)), smem, stream);
     lc.attrs[1].id = cudaLaunchAttributeClusterDimension;
-    lc.attrs[1].val.clusterDim.x = kClusterSplits;
+    lc.attrs[1].val.clusterDim.x = (unsigned)p.cl;
     lc.attrs[1].val.clusterDim.y = 1;
     lc.attrs[1].val.clusterDim.z = 1;
     lc.cfg.numAttrs = 2;
@@ -796,8 +806,8 @@ bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
 
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
                           int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
-                          float *part, int n_splits, int tokens_per_split, const void *k_new,
-                          const void *v_new, cudaStream_t stream) {
+                          float *part, int n_splits, int tokens_per_split, int cluster,
+                          const void *k_new, const void *v_new, cudaStream_t stream) {
     MmaParams p;
     p.kc = make_view(k);
     p.vc = make_view(v);
@@ -836,7 +846,8 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     const size_t qbytes = q_bytes(n_q_heads, nb);
     p.stages = (int)std::min<size_t>(4, (kSmemBudget - qbytes - 128) / stage);
     if (p.stages < 2) return TQ_ERR_UNSUPPORTED;
-    if (n_splits % kClusterSplits) return TQ_ERR_UNSUPPORTED;
+    if (cluster < 1 || cluster > kClusterSplits || n_splits % cluster) return TQ_ERR_UNSUPPORTED;
+    p.cl = cluster;
     const size_t cpart = (size_t)n_q_heads * part_stride(k.head_dim) * sizeof(float);
     if (cpart > (size_t)p.stages * stage) return TQ_ERR_UNSUPPORTED;
     p.cpart_offset = (int)(((size_t)p.stages * stage - cpart) & ~size_t(15));

@@ -18,8 +18,10 @@ constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
 
 __host__ __device__ constexpr int block_bytes(int type) { return 2 + kBlock * type / 8; }
 
-// Split-K CTAs of one cluster: the tensor-core attention kernel merges the partials of
-// these consecutive splits in distributed shared memory before writing one row.
+// Split-K CTAs of one cluster for a single sequence: the tensor-core attention kernel merges
+// the partials of these consecutive splits in distributed shared memory before writing one
+// row.  Batches run without pairs (in a batch of mixed lengths a pair often joins a split
+// with work to an empty one, which then holds its SM until its partner is done).
 constexpr int kClusterSplits = 2;
 
 // Floats per split-partial row of one (sequence, split, query head): head_dim rotated-domain
@@ -211,10 +213,12 @@ tq_status launch_append(const tq_cache &k, const tq_cache &v, const void *k_new,
 
 // Tensor-core decode attention (tq_attn_mma.cu): writes split partials like the fp32 kernel.
 bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads);
+// `cluster` consecutive splits (2 or 1) merge their partials in distributed shared memory;
+// the kernel writes n_splits / cluster partial rows per (sequence, head).
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
                           int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
-                          float *part, int n_splits, int tokens_per_split, const void *k_new,
-                          const void *v_new, cudaStream_t stream);
+                          float *part, int n_splits, int tokens_per_split, int cluster,
+                          const void *k_new, const void *v_new, cudaStream_t stream);
 
 // Fault injection of tq_inject_wait_timeout (tq_attn_mma.cu).
 tq_status inject_wait_timeout(int n_calls);
