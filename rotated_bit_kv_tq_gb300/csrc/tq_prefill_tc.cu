@@ -85,6 +85,7 @@ struct TcParams {
     int32_t chunked_k, chunked_v;
     float score_scale;      // softmax scale * log2(e) / (sqrt(128) * h_scale of the K table)
     float out_scale;        // 1 / (sqrt(128) * h_scale of the V table)
+    int32_t split;          // CTAs per query block: 1, or 2 (a cluster: key tiles cut in two halves)
 };
 
 struct TcSmem {
@@ -233,6 +234,27 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity) {
     record_error(TQ_ERR_DEVICE_TIMEOUT);
     return false;
 }
+// Cluster-wide barrier, each thread on its own (not warp-aligned): every thread of both CTAs
+// of a split query block passes it exactly twice (before and after the partial exchange).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
+    uint32_t ra;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t local, uint32_t rank) {
+    uint32_t ra;
+    float4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(ra) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -348,14 +370,14 @@ __device__ __forceinline__ void fwht64(float (&x)[64]) {
 // P V has completed).
 template <int TYPE, bool IS_V>
 __device__ __forceinline__ void tc_produce(const TcParams &p, TcSmem &sm, int g, int64_t n_keys,
-                                           int n_tiles, int pt, volatile int *abort_v) {
+                                           int tile0, int n_tiles, int pt, volatile int *abort_v) {
     const CacheView &cv = IS_V ? p.vc : p.kc;
     const bool chunked = IS_V ? p.chunked_v : p.chunked_k;
     uint8_t *raw = sm.raw[IS_V ? 1 : 0];
     uint8_t *ok = sm.ok[IS_V ? 1 : 0];
     const HalfTables tab = make_tables<TYPE>();
     const int free_bar = IS_V ? kBarPvFree : kBarSFree, full_bar = IS_V ? kBarVFull : kBarKFull;
-    if (n_tiles > 0) tc_stage<TYPE>(cv, p.seq, chunked, raw, ok, g, 0, n_keys, pt);
+    if (n_tiles > 0) tc_stage<TYPE>(cv, p.seq, chunked, raw, ok, g, (int64_t)tile0 * kTcKeys, n_keys, pt);
     cp_async_commit();
     for (int i = 0; i < n_tiles; ++i) {
         const int b = i & 1;
@@ -367,7 +389,7 @@ __device__ __forceinline__ void tc_produce(const TcParams &p, TcSmem &sm, int g,
         else tc_decode<TYPE, false>(raw, ok, g, tab, sm.k[b], sm.kn[b], pt);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_arrive(smem_u32(&sm.bar[full_bar + b]));
-        if (i + 1 < n_tiles) tc_stage<TYPE>(cv, p.seq, chunked, raw, ok, g, (int64_t)(i + 1) * kTcKeys, n_keys, pt);
+        if (i + 1 < n_tiles) tc_stage<TYPE>(cv, p.seq, chunked, raw, ok, g, (int64_t)(tile0 + i + 1) * kTcKeys, n_keys, pt);
         cp_async_commit();
     }
     cp_async_wait<0>();
@@ -383,13 +405,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
     TcSmem &sm = *reinterpret_cast<TcSmem *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     __shared__ int abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // CTAs run longest first: the last query block (the most keys) of every head first
-    const int g = (int)(blockIdx.x % (unsigned)p.n_kv_heads), G = p.group, Hq = p.n_q_heads;
-    const int64_t j0 = (p.n_qblocks - 1 - (int64_t)(blockIdx.x / (unsigned)p.n_kv_heads)) * p.bq;
+    // CTAs run longest first: the last query block (the most keys) of every head first.  With
+    // split = 2, the two CTAs of a cluster share a query block: rank 0 takes the first half of
+    // its key tiles, rank 1 the rest, and they merge their partial outputs at the end.
+    const unsigned qcta = p.split == 2 ? blockIdx.x >> 1 : blockIdx.x;
+    const int rank = p.split == 2 ? (int)(blockIdx.x & 1u) : 0;   // the cluster rank
+    const int g = (int)(qcta % (unsigned)p.n_kv_heads), G = p.group, Hq = p.n_q_heads;
+    const int64_t j0 = (p.n_qblocks - 1 - (int64_t)(qcta / (unsigned)p.n_kv_heads)) * p.bq;
     const int64_t j_end = min64(p.n_q, j0 + p.bq);
     const int64_t n_keys = p.pos0 + j_end;                  // rows the CTA's last query sees
     const int64_t first_pos = p.pos0 + j0;                  // the CTA's first query position
-    const int n_tiles = (int)((n_keys + kTcKeys - 1) / kTcKeys);
+    const int n_all = (int)((n_keys + kTcKeys - 1) / kTcKeys);
+    const int half_tiles = (n_all + 1) / 2;
+    const int tile0 = p.split == 2 && rank == 1 ? half_tiles : 0;          // first key tile
+    const int n_tiles = p.split == 2 ? (rank == 0 ? half_tiles : n_all - half_tiles) : n_all;
     auto bar = [&](int i) { return smem_u32(&sm.bar[i]); };
 
     if (tid == 0) {
@@ -486,7 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = m_run;
-            if ((int64_t)i * kTcKeys + (kTcKeys - 1) <= first_pos) {
+            if ((int64_t)(tile0 + i) * kTcKeys + (kTcKeys - 1) <= first_pos) {
                 // every key of the tile is visible to every row of the CTA
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
@@ -495,7 +524,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
                 }
             } else {
                 // keys past this row's position are masked
-                const int64_t t0 = (int64_t)i * kTcKeys + 64 * h;
+                const int64_t t0 = (int64_t)(tile0 + i) * kTcKeys + 64 * h;
                 const int lim = (int)max64(-1, min64(qpos - t0, 64));   // keys j > lim are masked
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
@@ -565,7 +594,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         tc_fence_after();
         sm.xch[n_tiles & 1][h][r] = l_run;   // slot of tile n_tiles - 2: the partner is past it
         float o[64];
-        tc_ld64(tmem + lane_base + kTmemO + 64u * h, o);
+        if (n_tiles > 0) {
+            tc_ld64(tmem + lane_base + kTmemO + 64u * h, o);
+        } else {   // a key range with no tiles (split, one-tile prompt): nothing was accumulated
+#pragma unroll
+            for (int e = 0; e < 64; ++e) o[e] = 0.f;
+        }
         fwht64(o);   // strides 1 .. 32 of this half
         // the stride-64 butterfly pairs coord c with c + 64: the halves swap through the K
         // tile area, idle once every MMA has completed (float4 chunks XOR-swizzled by row)
@@ -576,29 +610,70 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
             *reinterpret_cast<float4 *>(xo_at(r, 16 * h + c)) =
                 make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         named_sync(pair_bar, 64);
-        const float l_row = l_run + sm.xch[n_tiles & 1][h ^ 1][r];
-        if (valid && done) {
+        float l_row = l_run + sm.xch[n_tiles & 1][h ^ 1][r];
+        // y: coords 64 h .. 64 h + 63 of the rotated-back row, before the division by l
+        // (h = 0: coord c' = o + partner (coords c', c' + 64); h = 1: partner - o)
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const float4 u = *reinterpret_cast<const float4 *>(xo_at(r, 16 * (h ^ 1) + c));
+            const float pv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[4 * c + e] = h ? pv[e] - o[4 * c + e] : o[4 * c + e] + pv[e];
+        }
+        bool write = valid && done;
+        if (p.split == 2) {
+            // The two CTAs of the query block merge by log-sum-exp: the CTA of rank h finishes
+            // coords 64 h .. of every row; the thread of the other half publishes its coords and
+            // the row's (max, sum) in the V tile area (idle after the last P V) for the partner.
+            float *X = reinterpret_cast<float *>(sm.v[0]);                 // [row][64]
+            float *Xml = reinterpret_cast<float *>(sm.v[1]);               // [row][2]
+            const float m_row = n_tiles > 0 ? m_run : -INFINITY;
+            if (h != rank) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    *reinterpret_cast<float4 *>(X + r * 64 + 4 * c) =
+                        make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                Xml[2 * r] = m_row;
+                Xml[2 * r + 1] = l_row;
+            }
+            cluster_sync_all();
+            if (h == rank) {
+                const uint32_t peer = (uint32_t)(rank ^ 1);
+                const float mp = ld_cluster_f32(smem_u32(Xml + 2 * r), peer);
+                const float lp = ld_cluster_f32(smem_u32(Xml + 2 * r + 1), peer);
+                const float M = fmaxf(m_row, mp);
+                const float wa = m_row == -INFINITY ? 0.f : ex2(m_row - M);
+                const float wb = mp == -INFINITY ? 0.f : ex2(mp - M);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float4 u = ld_cluster_f32x4(smem_u32(X + r * 64 + 4 * c), peer);
+                    o[4 * c] = wa * o[4 * c] + wb * u.x;
+                    o[4 * c + 1] = wa * o[4 * c + 1] + wb * u.y;
+                    o[4 * c + 2] = wa * o[4 * c + 2] + wb * u.z;
+                    o[4 * c + 3] = wa * o[4 * c + 3] + wb * u.w;
+                }
+                l_row = wa * l_row + wb * lp;
+            }
+            cluster_sync_all();   // the partner has read this CTA's exchange area
+            write = valid && h == rank && !*abort_v;
+        }
+        if (write) {
             const float inv = l_row > 0.f ? p.out_scale / l_row : 0.f;
             float4 *dst = reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)kBlock + 64 * h);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const float4 u = *reinterpret_cast<const float4 *>(xo_at(r, 16 * (h ^ 1) + c));
-                const float pv[4] = {u.x, u.y, u.z, u.w};
                 float v4[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    // h = 0: coord c' = o + partner (coords c', c' + 64); h = 1: partner - o
-                    const float y = h ? pv[e] - o[4 * c + e] : o[4 * c + e] + pv[e];
-                    v4[e] = __uint_as_float(__float_as_uint(y * inv) ^ sign_mask(p.vc, 64 * h + 4 * c + e));
-                }
+                for (int e = 0; e < 4; ++e)
+                    v4[e] = __uint_as_float(__float_as_uint(o[4 * c + e] * inv) ^ sign_mask(p.vc, 64 * h + 4 * c + e));
                 dst[c] = make_float4(v4[0], v4[1], v4[2], v4[3]);
             }
         }
     } else if (warp < kTcMmaWarp) {
         // ================= producers: warps 8-11 the K cache, 12-15 the V cache
         const int pt = (tid - kTcSoftmax) & (kTcGroup - 1);
-        if (tid - kTcSoftmax < kTcGroup) tc_produce<TK, false>(p, sm, g, n_keys, n_tiles, pt, abort_v);
-        else tc_produce<TV, true>(p, sm, g, n_keys, n_tiles, pt, abort_v);
+        if (tid - kTcSoftmax < kTcGroup) tc_produce<TK, false>(p, sm, g, n_keys, tile0, n_tiles, pt, abort_v);
+        else tc_produce<TV, true>(p, sm, g, n_keys, tile0, n_tiles, pt, abort_v);
     } else if (lane == 0) {
         // ================= MMA issue (one thread)
         constexpr uint32_t idesc_s = idesc_f16(false), idesc_pv = idesc_f16(true);
@@ -653,6 +728,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         tc_commit(bar(kBarDrain));   // arrives once everything issued above has completed
         tc_wait(bar(kBarDrain), 0);
     }
+    // the other roles pass the two cluster barriers of the softmax warps' partial exchange
+    if (p.split == 2 && warp >= kTcSoftmax / 32) {
+        cluster_sync_all();
+        cluster_sync_all();
+    }
     // teardown: every MMA has completed (the softmax waited for the last P V, or all roles
     // gave up on a timeout); release the tensor memory
     tc_fence_before();
@@ -668,7 +748,14 @@ tq_status launch_tc_t(const TcParams &p, unsigned n_ctas, cudaStream_t stream) {
     const tq_status st = kernel_setup(reinterpret_cast<const void *>(prefill_tc_kernel<TK, TV>),
                                       (int)smem, kTcThreads, nullptr);
     if (st != TQ_OK) return st;
-    PdlConfig lc(dim3(n_ctas), dim3(kTcThreads), smem, stream);
+    PdlConfig lc(dim3(n_ctas * (unsigned)p.split), dim3(kTcThreads), smem, stream);
+    if (p.split == 2) {   // the two CTAs of a query block form a cluster
+        lc.attrs[1].id = cudaLaunchAttributeClusterDimension;
+        lc.attrs[1].val.clusterDim.x = 2;
+        lc.attrs[1].val.clusterDim.y = 1;
+        lc.attrs[1].val.clusterDim.z = 1;
+        lc.cfg.numAttrs = 2;
+    }
     return check_cuda(cudaLaunchKernelEx(&lc.cfg, prefill_tc_kernel<TK, TV>, p));
 }
 
@@ -704,8 +791,20 @@ tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, in
     p.n_kv_heads = k.n_kv_heads;
     p.n_qblocks = (n_q + p.bq - 1) / p.bq;
     const int64_t n_ctas = p.n_qblocks * k.n_kv_heads;
-    if (n_ctas > 0x7fffffff) return TQ_ERR_UNSUPPORTED;
+    if (n_ctas > 0x3fffffff) return TQ_ERR_UNSUPPORTED;
     const unsigned nc = (unsigned)n_ctas;
+    // Split each query block's key tiles over a cluster of two CTAs when that fills the last
+    // wave of one-CTA-per-SM launches markedly better (the two CTAs both rotate the queries,
+    // so a split costs a little): e.g. the 512 CTAs of a 2,048-token chunk of a Llama-shape
+    // prompt run 3.37 waves on 152 SMs (84 % of the last wave's SMs busy over the launch), and
+    // 1,024 half-length CTAs run 6.74 (96 %).
+    {
+        const double sms = (double)device_sm_count();
+        const double w1 = (double)n_ctas / sms, w2 = 2.0 * w1;
+        const double e1 = w1 / std::ceil(w1), e2 = w2 / std::ceil(w2);
+        const int64_t max_tiles = (pos0 + n_q + kTcKeys - 1) / kTcKeys;
+        p.split = (max_tiles >= 4 && e2 > 1.08 * e1) ? 2 : 1;
+    }
     if (k.type == TQ_TURBO3 && v.type == TQ_TURBO3) return launch_tc_t<3, 3>(p, nc, stream);
     if (k.type == TQ_TURBO2 && v.type == TQ_TURBO2) return launch_tc_t<2, 2>(p, nc, stream);
     if (k.type == TQ_TURBO3 && v.type == TQ_TURBO2) return launch_tc_t<3, 2>(p, nc, stream);

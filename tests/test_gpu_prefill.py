@@ -139,3 +139,35 @@ def test_prefill_full_size_llama_chunk_sampled(tq):
     for j in (0, 1, 257, n_q - 1):
         ref = oracle.attn_decode(3, 3, kr, vr, q[j], pos0 + j + 1, 32, 8, 128, 1 / np.sqrt(128))
         _check(got[j][None], ref[None], f"prefill llama3-8b 32K last chunk#{j}")
+
+
+SPLIT_CASES = [
+    # (tk, tv, n_kv_heads, n_q_heads, pos0, n_q): shapes whose one-CTA-per-query-block grid
+    # fills the last wave of 152 SMs poorly, so the key tiles of each query block are split
+    # over a cluster of two CTAs (merged by log-sum-exp)
+    (3, 3, 8, 32, 400, 250),   # 64 CTAs -> 128; 6 key tiles per block, 3 per CTA
+    (3, 2, 2, 8, 0, 600),      # 38 CTAs -> 76; block 0 sees one key tile (its second CTA none)
+    (2, 2, 4, 20, 517, 130),   # G 5 (25 queries per block), odd tile counts (5 / 6)
+]
+
+
+@pytest.mark.parametrize("tk,tv,hkv,hq,pos0,n_q", SPLIT_CASES)
+def test_prefill_split_key_range_matches_oracle(tq, tk, tv, hkv, hq, pos0, n_q):
+    w = synth.scaled(synth.TINY, n_kv_heads=hkv, n_q_heads=hq, head_dim=128)
+    n_rows = pos0 + n_q
+    k = synth.kv_tokens(w, 1, "K", 0, n_rows).reshape(n_rows, -1)
+    v = synth.kv_tokens(w, 1, "V", 0, n_rows).reshape(n_rows, -1)
+    kc = tq.KVCache(tk, hkv, 128, capacity_tokens=n_rows)
+    vc = tq.KVCache(tv, hkv, 128, capacity_tokens=n_rows)
+    tq.encode(kc, torch.from_numpy(k).to(DEV))
+    tq.encode(vc, torch.from_numpy(v).to(DEV))
+    q = _queries(w, 1, pos0, n_q)
+    out = torch.full((n_q, hq, 128), float("nan"), device=DEV)
+    tq.attn_prefill(kc, vc, torch.from_numpy(q).to(DEV), out, pos0=pos0)
+    assert tq.device_status() == 0
+    kr = kc.buffer.cpu().numpy().reshape(n_rows, -1)
+    vr = vc.buffer.cpu().numpy().reshape(n_rows, -1)
+    ref = oracle.attn_prefill(tk, tv, kr, vr, q, pos0, hkv, 128, 1 / np.sqrt(128))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    _check(got, ref, f"prefill split turbo{tk}/{tv} Hkv{hkv} Hq{hq}#{pos0}+{n_q}")
