@@ -56,8 +56,12 @@ BENCH_WORKLOADS = [synth.LLAMA3_8B_32K, synth.QWEN25_14B_32K, synth.HD256_128K,
 # benchmark's own shapes; see the profile summaries.  A workload without a capture of the
 # current kernels reports null.
 TRAFFIC = {
-    # (workload, type): {"attn": bytes per tq_attn_decode_append launch at the bench's final
-    # context, "encode": bytes per tq_encode_kv launch of one layer's prefill}
+    # (workload, type): {"attn_per_token": DRAM bytes of one tq_attn_decode_append launch per
+    # context token (the launch reads every packed row once, so traffic grows with the
+    # context), "encode": DRAM bytes of one tq_encode_kv launch of one layer's prefill}
+    # Llama-3-8B shape, turbo3: `--kernel-probe 32768` captures of the decode-step and encode
+    # kernels under ncu; the encode capture is the benchmark's own launch size.
+    ("llama3-8b-kv-32k", 3): {"attn_per_token": 26323456 / 32768, "encode": 134294528 + 10227968},
 }
 
 
@@ -76,6 +80,12 @@ def parse():
     ap.add_argument("--kernel-probe", type=int, default=0, metavar="CTX",
                     help="time one layer's encode and attention at context CTX (the small "
                          "case the ncu captures use) instead of the full benchmark")
+    ap.add_argument("--probe-kv-heads", type=int, default=0, metavar="N",
+                    help="kernel probe on N KV heads (same query heads per KV head), e.g. 3 for "
+                         "150-byte rows, a shape only the fp32 CUDA-core kernel takes")
+    ap.add_argument("--prefill-chunk", type=int, default=0, metavar="N",
+                    help="prefill probe: the last N queries of the CTX-token prompt as one chunk "
+                         "(default: the whole prompt)")
     ap.add_argument("--phase-trace", type=int, default=0, metavar="CTX",
                     help="per-phase globaltimer trace of the decode step (traced library, "
                          "32 layers of the workload's shape at context CTX, graph replay)")
@@ -533,6 +543,8 @@ def run_ours(args, w, tt, rank, world, local_rank, dist, cpu_baseline_on):
     e_bytes = encode_bytes_per_token(w, tt) * prompt_tokens      # K and V of one layer
     e_gbs = e_bytes / (enc_launch_ms / 1e3) / 1e9
     traffic = TRAFFIC.get((w.name, tt), {})
+    attn_traffic = (traffic["attn_per_token"] * float(final_ctx.sum())
+                    if "attn_per_token" in traffic else None)
     decode_gb = attn_bytes_batch(w, lens0 + S // 2, tt) * L / 1e9
     line = {
         "metric": METRIC,
@@ -562,7 +574,7 @@ def run_ours(args, w, tt, rank, world, local_rank, dist, cpu_baseline_on):
                      "bound": "hbm",
                      "achieved": a_gbs, "peak": peak, "unit": "GB/s", "frac": a_gbs / peak,
                      "peak_source": peak_kind,
-                     "traffic": traffic.get("attn"),
+                     "traffic": attn_traffic,
                      "bytes_per_launch": a_bytes, "launch_ms": attn_launch_ms},
         "encode_roofline": {"kernel": "tq_encode_kv (prefill, one layer, K and V)", "bound": "hbm",
                             "achieved": e_gbs, "peak": peak, "unit": "GB/s", "frac": e_gbs / peak,
@@ -701,6 +713,8 @@ def kernel_probe(args):
     from rotated_bit_kv_tq_gb300 import build
     build.build()
     w = workload(args.workload)
+    if args.probe_kv_heads:
+        w = synth.scaled(w, n_kv_heads=args.probe_kv_heads, n_q_heads=w.group * args.probe_kv_heads)
     tt = w.types[0]
     tq.codebook_init(tt, 0)
     ctx, Hkv, Hq, D = args.kernel_probe, w.n_kv_heads, w.n_q_heads, w.head_dim
@@ -846,7 +860,8 @@ def phase_trace(args):
 
 def prefill_probe(args):
     """One layer of the workload's shape: encode a CTX-token prompt's K and V, then run the
-    whole prompt as one causal chunk; per-call times from CUDA events (not a bench line)."""
+    whole prompt (or its last --prefill-chunk queries) as one causal chunk; per-call times from
+    CUDA events (not a bench line)."""
     import torch
     import rotated_bit_kv_tq_gb300 as tq
     from rotated_bit_kv_tq_gb300 import build
@@ -860,20 +875,22 @@ def prefill_probe(args):
     kc = tq.KVCache(tt, Hkv, D, capacity_tokens=ctx)
     vc = tq.KVCache(tt, Hkv, D, capacity_tokens=ctx)
     tq.encode_kv(kc, vc, k16, v16)
-    q = torch.randn(ctx, Hq, D, generator=torch.Generator().manual_seed(5)).half().cuda()
-    out = torch.empty(ctx, Hq, D, device="cuda")
+    n_q = args.prefill_chunk or ctx
+    pos0 = ctx - n_q
+    q = torch.randn(n_q, Hq, D, generator=torch.Generator().manual_seed(5)).half().cuda()
+    out = torch.empty(n_q, Hq, D, device="cuda")
     for _ in range(3):
-        tq.attn_prefill(kc, vc, q, out, pos0=0)
+        tq.attn_prefill(kc, vc, q, out, pos0=pos0)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(5):
-        tq.attn_prefill(kc, vc, q, out, pos0=0)
+        tq.attn_prefill(kc, vc, q, out, pos0=pos0)
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / 5
-    print(json.dumps({"probe": w.name, "prompt": ctx, "prefill_us": ms * 1e3,
-                      "tflops": prefill_flops(Hq, D, 0, ctx) / ms / 1e9,
+    print(json.dumps({"probe": w.name, "prompt": ctx, "chunk": n_q, "pos0": pos0,
+                      "prefill_us": ms * 1e3, "tflops": prefill_flops(Hq, D, pos0, n_q) / ms / 1e9,
                       "status": tq.device_status()}))
 
 

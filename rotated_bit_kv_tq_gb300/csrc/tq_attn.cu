@@ -413,8 +413,12 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
 constexpr int kMergeWarpRows = 16;   // rows one warp merges in its single round of loads
 
 __global__ void __launch_bounds__(256) attn_merge_warp_kernel(const AttnParams p) {
+    const int trace_slot = kTraceCtas + blockIdx.y * gridDim.x + blockIdx.x;   // phase trace only
+    (void)trace_slot;
+    if (threadIdx.x == 0) TQ_PHASE(trace_slot, 0);
     pdl_wait();
     pdl_launch_dependents();
+    if (threadIdx.x == 0) TQ_PHASE(trace_slot, 1);
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * 8 + (threadIdx.x >> 5);   // (head, block) of sequence blockIdx.y
     const int D = p.head_dim, Hq = p.n_q_heads;
@@ -447,11 +451,13 @@ __global__ void __launch_bounds__(256) attn_merge_warp_kernel(const AttnParams p
         o4[2] = fmaf(wr, v[r].z, o4[2]);
         o4[3] = fmaf(wr, v[r].w, o4[3]);
     }
+    if (threadIdx.x == 0 && o4[0] != o4[0] + 1.0f) TQ_PHASE(trace_slot, 2);   // loads consumed
     const float inv = L > 0.f ? kInvSqrt128 / L : 0.f;
     warp_fwht4(o4, lane);                    // inverse rotation (1/sqrt(128)) W o_b
     apply_signs4(o4, p.vc, 4 * lane);        // inverse D W of the V cache
     *reinterpret_cast<float4 *>(p.out + (seq * Hq + h) * D + b * kBlock + 4 * lane) =
         make_float4(o4[0] * inv, o4[1] * inv, o4[2] * inv, o4[3] * inv);
+    if (lane == 0) TQ_PHASE(trace_slot, 3);
 }
 
 size_t partial_smem(const AttnParams &p) {
