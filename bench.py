@@ -758,10 +758,14 @@ def kernel_probe(args):
 
 
 TRACE_PHASES = {
-    "attention": ["entry", "dependency wait returned", "sequence length loaded",
-                  "first tile requested", "query rotated (CTA barrier)", "first tile landed",
-                  "loop end (slowest warp)", "epilogue done (cluster barrier)",
-                  "cluster merge done"],
+    "attention": ["entry", "dependency wait returned",
+                  "sequence length loaded (a full first tile requested)",
+                  "set-up done (any other first tile requested)", "query rotated (CTA barrier)",
+                  "first tile landed",
+                  "loop end (slowest warp)",
+                  "epilogue done (cluster barrier; grid merge: partial rows stored)",
+                  "cluster merge done (grid merge: grid barrier passed)",
+                  "grid merge: rows loaded", "grid merge: output stored"],
     "merge": ["entry", "dependency wait returned", "partial rows loaded", "output stored"],
 }
 

@@ -179,10 +179,18 @@ TQ_API size_t tq_attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim,
  *   softmax_scale  score scale; pass 0 for 1/sqrt(head_dim)
  *   out            device fp32 [n_seqs][n_q_heads][head_dim]
  *   workspace      device scratch of at least tq_attn_workspace_bytes(...) bytes,
- *                  16-byte aligned; contents need no initialisation
+ *                  16-byte aligned; contents need no initialisation.  Its first 4 KiB
+ *                  hold an epoch word that the next call on the same workspace reads
+ *                  (see below), so calls that share a workspace must be ordered (one
+ *                  stream, or events), as they must be for the partials anyway.
  * The scores are computed as |k| * (W q / sqrt(128)) . c(codes) and the values
  * accumulated as sum p |v| c(codes), both in the rotated domain, with one inverse
- * FWHT per output block; no fp16 K or V is formed. */
+ * FWHT per output block; no fp16 K or V is formed.  The keys are split over the SMs
+ * (split-K) and the partial results merged by log-sum-exp.  On the tensor-core path a
+ * single sequence whose splits fit one wave is one cooperative launch: its CTAs merge the
+ * partials themselves, each partial value stored with a tag derived from the epoch word
+ * (which the launch advances), so that a reader knows a current value from a stale one
+ * without a grid barrier.  Otherwise a merge kernel follows the attention kernel. */
 TQ_API tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void *q_f16,
                          int n_seqs, int n_q_heads, const int32_t *seq_lens,
                          int64_t max_seq_len, float softmax_scale, float *out,
@@ -198,8 +206,9 @@ TQ_API tq_status tq_attn_decode(const tq_cache *k, const tq_cache *v, const void
  *                  seq_lens[s] == 0 appends nothing and gets a zero output.
  *   other arguments as for tq_attn_decode; seq_lens counts the appended token.
  * On the tensor-core path the CTA whose split holds position seq_lens[s] - 1 encodes the
- * rows itself, so the step is one attention launch plus the merge; shapes that path does
- * not take append in a launch of their own first.  A row whose position the cache cannot
+ * rows itself, so the step is one attention launch (plus the merge kernel where
+ * tq_attn_decode has one); shapes that path does not take append in a launch of their own
+ * first.  A row whose position the cache cannot
  * address is skipped and TQ_ERR_OUT_OF_RANGE is recorded for tq_device_status. */
 TQ_API tq_status tq_attn_decode_append(const tq_cache *k, const tq_cache *v,
                                        const void *k_new_f16, const void *v_new_f16,
@@ -251,7 +260,8 @@ TQ_API tq_status tq_attn_prefill(const tq_cache *k, const tq_cache *v, const voi
  *   followed.  The first call on a device loads the library's device code there; make
  *   that first call before any stream capture.
  *   Sharing: all calls on a device share the array and it keeps the last call's
- *   contents (each call writes every partial it reads, so nothing needs clearing).
+ *   contents (each call writes every partial it reads, so nothing needs clearing; the
+ *   epoch word of tq_attn_decode's workspace lives in it too).
  *   Calls whose kernels overlap on the GPU (different streams without ordering) race on
  *   it; order them on one stream or with events. */
 TQ_API tq_status tq_attn_decode_noalloc(const tq_cache *k, const tq_cache *v,

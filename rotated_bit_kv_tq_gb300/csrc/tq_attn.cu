@@ -323,16 +323,22 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     const int trace_slot = kTraceCtas + blockIdx.y * gridDim.x + blockIdx.x;   // phase trace only
     (void)trace_slot;
     if (threadIdx.x == 0) TQ_PHASE(trace_slot, 0);
-    // launched as a programmatic dependent of the partial kernel: wait for its results
-    pdl_wait();
-    pdl_launch_dependents();
-    if (threadIdx.x == 0) TQ_PHASE(trace_slot, 1);
     __shared__ float red_m[8], red_l[8];
     __shared__ float4 red_o[8][32];
     const int h = blockIdx.x, seq = blockIdx.y, b = blockIdx.z, D = p.head_dim;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *base = p.part + ((int64_t)seq * p.n_splits * p.n_q_heads + h) * part_stride(D);
     const int64_t sstride = (int64_t)p.n_q_heads * part_stride(D);
+    // the rows of this warp's first round into L2 while the partial kernel finishes
+    if (lane < kMergeRows && warp + 8 * lane < p.n_splits) {
+        const float *row = base + (warp + 8 * lane) * sstride;
+        l2_prefetch(row + b * kBlock, kBlock * sizeof(float));
+        l2_prefetch(row + D, 4 * sizeof(float));
+    }
+    // launched as a programmatic dependent of the partial kernel: wait for its results
+    pdl_wait();
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) TQ_PHASE(trace_slot, 1);
     // One pass: warp w takes splits w, w + 8, ...; all rows of a round are loaded before
     // any is used, and the warp's running maximum rescales what it has summed so far.
     float M = -INFINITY, lsum = 0.f;
@@ -416,18 +422,24 @@ __global__ void __launch_bounds__(256) attn_merge_warp_kernel(const AttnParams p
     const int trace_slot = kTraceCtas + blockIdx.y * gridDim.x + blockIdx.x;   // phase trace only
     (void)trace_slot;
     if (threadIdx.x == 0) TQ_PHASE(trace_slot, 0);
-    pdl_wait();
-    pdl_launch_dependents();
-    if (threadIdx.x == 0) TQ_PHASE(trace_slot, 1);
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * 8 + (threadIdx.x >> 5);   // (head, block) of sequence blockIdx.y
     const int D = p.head_dim, Hq = p.n_q_heads;
-    if (item >= Hq * p.nb) return;
     const int b = item % p.nb, h = item / p.nb;
     const int64_t seq = blockIdx.y;
     const int R = p.n_splits;
     const float *base = p.part + (seq * R * Hq + h) * part_stride(D);
     const int64_t sstride = (int64_t)Hq * part_stride(D);
+    // this warp's rows into L2 while the partial kernel finishes
+    if (item < Hq * p.nb && lane < R) {
+        const float *row = base + lane * sstride;
+        l2_prefetch(row + b * kBlock, kBlock * sizeof(float));
+        l2_prefetch(row + D, 4 * sizeof(float));
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) TQ_PHASE(trace_slot, 1);
+    if (item >= Hq * p.nb) return;
     float2 ml = make_float2(-INFINITY, 0.f);
     if (lane < R) ml = *reinterpret_cast<const float2 *>(base + lane * sstride + D);
     float4 v[kMergeWarpRows];
@@ -494,7 +506,10 @@ tq_status launch_attn_t(const AttnParams &p, int n_seqs, cudaStream_t stream) {
 size_t attn_workspace_bytes(int n_seqs, int n_q_heads, int head_dim, int64_t max_seq_len,
                             int sm_count) {
     const SplitPlan pl = plan_splits(n_seqs, head_dim, max_seq_len, sm_count);
-    return sizeof(float) * (size_t)n_seqs * pl.n_splits * n_q_heads * part_stride(head_dim);
+    const size_t rows = sizeof(float) * (size_t)n_seqs * pl.n_splits * n_q_heads * part_stride(head_dim);
+    // the grid merge of one sequence keeps every value with a 32-bit tag (64-bit words)
+    const bool grid = n_seqs == 1 && pl.n_splits <= std::min(sm_count, kGridMergeMaxCtas);
+    return kGridBarrierBytes + (grid ? 2 : 1) * rows;
 }
 
 tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
@@ -506,7 +521,8 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
     p.vc = make_view(v);
     p.q = static_cast<const __half *>(q);
     p.seq_lens = seq_lens;
-    p.part = static_cast<float *>(ws);
+    // the grid-merge area, then the partial rows
+    p.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kGridBarrierBytes);
     p.out = out;
     p.scale = scale;
     p.max_len = max_seq_len;
@@ -525,11 +541,16 @@ tq_status launch_attn(const tq_cache &k, const tq_cache &v, const void *q, int n
                                         device_sm_count()))
         return TQ_ERR_WORKSPACE_TOO_SMALL;
     if (attn_mma_supported(k, v, n_q_heads)) {
-        const int cluster = n_seqs == 1 ? kClusterSplits : 1;
+        // One wave of CTAs merges its own partials after a grid barrier (no merge kernel, no
+        // kernel boundary before the output); otherwise a single sequence pairs its splits
+        // in clusters, and the merge kernel follows.
+        const bool grid = grid_merge_fits(n_seqs, p.n_splits);
+        const int cluster = grid ? 1 : n_seqs == 1 ? kClusterSplits : 1;
         tq_status st = launch_attn_mma(k, v, q, n_seqs, n_q_heads, seq_lens, max_seq_len, scale,
                                        p.part, p.n_splits, p.tokens_per_split, cluster, k_new,
-                                       v_new, stream);
-        if (st != TQ_OK) return st;
+                                       v_new, grid ? out : nullptr,
+                                       grid ? static_cast<uint64_t *>(ws) : nullptr, stream);
+        if (st != TQ_OK || grid) return st;
         AttnParams pm = p;
         pm.n_splits = p.n_splits / cluster;   // one partial row per cluster
         return launch_merge(pm, n_seqs, stream);

@@ -52,6 +52,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kWaitLimit = 1u << 26;  // bounded mbarrier wait (tens of ms)
 constexpr uint32_t kInjectedWaitLimit = 64;   // polls per wait under tq_inject_wait_timeout
+constexpr uint32_t kGridWaitLimit = 1u << 16;  // grid-merge polls (each an L2 round trip)
+constexpr uint32_t kEpochMark = 0x7154e90cu;   // high half of an epoch word this form wrote
 
 // Launches still to run with injected timeouts (tq_inject_wait_timeout).
 std::atomic<int> g_inject_timeouts{0};
@@ -86,6 +88,10 @@ struct MmaParams {
     int32_t cpart_offset;   // bytes from the first stage to this CTA's partial rows
     int32_t cl;             // CTAs per cluster: 2 (pairs of splits merge in shared memory) or 1
     uint32_t wait_limit;    // polls per bounded mbarrier wait
+    // grid merge (one wave, cooperative launch): the output and the barrier area, else null
+    float *out;
+    uint64_t *bar;          // [0] epoch of the next call, [1 + cta] arrival flags
+    uint32_t grid_wait_limit;   // polls of the grid barrier
     int32_t withhold_tiles; // fault injection: request no tile copies (every tile wait runs out)
     // 2, 4, 2^16, 2^30, 2^31: shift amounts as multipliers passed at run time, so that the
     // selector shifts compile to integer multiply-adds (FMA pipe) instead of ALU shifts
@@ -118,11 +124,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 }
 
 
-// Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
-__device__ __forceinline__ void l2_prefetch(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Issue the TMA bulk copies of one tile (rows [t0, t0+nt) of both caches) into a stage.
 // Runs of rows are split at page boundaries; every row run is a multiple of 16 bytes.
 __device__ __forceinline__ void issue_tile(const MmaParams &p, int seq, int64_t t0, int nt,
@@ -154,6 +155,20 @@ __device__ __forceinline__ void issue_tile(const MmaParams &p, int seq, int64_t 
 }
 
 
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t *a) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t *a, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+
+// (value, tag) as one 64-bit word: the value's bits low, the tag high
+__device__ __forceinline__ uint64_t tagged(float v, uint32_t tag) {
+    return ((uint64_t)tag << 32) | __float_as_uint(v);
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
@@ -163,6 +178,129 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     for (uint32_t it = 0; it < limit; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// The merge half of the grid merge, after this CTA's tagged partial rows are stored.
+template <int kConsumers>
+__device__ __forceinline__ void grid_merge(const float *part, uint64_t *bar, float *out, uint8_t *stage0,
+                                        uint64_t E, bool marked, uint32_t e, uint32_t tag, int Hq,
+                                        int D, int n_splits, uint32_t wait_limit, int trace_slot) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int PS = part_stride(D);
+    const int64_t rw = (int64_t)Hq * PS;
+    (void)trace_slot;
+    const int n_ctas = gridDim.x, me = blockIdx.x;
+    // merge scratch at the start of the (idle) ring; the partial rows above sit at its end
+    int *s_ok = reinterpret_cast<int *>(stage0);
+    float *s_red = reinterpret_cast<float *>(stage0) + 32;     // [2][kConsumers]
+    float *s_w = s_red + 2 * kConsumers;                       // [kGridMergeMaxCtas]
+    float *s_acc = s_w + kGridMergeMaxCtas;                    // [kConsumers][32]
+    if (!marked) {
+        if (warp == 0) {
+            const uint64_t token = (E + 1) * 0x9E3779B97F4A7C15ull;
+            if (lane == 0) {
+                __threadfence();   // this CTA's rows before its flag
+                st_relaxed_u64(bar + 1 + me, token);
+            }
+            bool all = false;
+            for (uint32_t it = 0; it < wait_limit && !all; ++it) {
+                uint64_t f[kGridMergeMaxCtas / 32];
+#pragma unroll
+                for (int k = 0; k < kGridMergeMaxCtas / 32; ++k) {
+                    const int c = lane + 32 * k;
+                    f[k] = c < n_ctas ? ld_relaxed_u64(bar + 1 + c) : token;
+                }
+                bool mine = true;
+#pragma unroll
+                for (int k = 0; k < kGridMergeMaxCtas / 32; ++k) mine &= f[k] == token;
+                all = __all_sync(0xffffffffu, mine);
+            }
+            __threadfence();   // the other CTAs' rows after their flags
+            if (lane == 0) *s_ok = all ? 1 : 0;
+        }
+        __syncthreads();
+        if (!*s_ok) {
+            if (tid == 0) record_error(TQ_ERR_DEVICE_TIMEOUT);
+            if (me == 0 && tid == 0) st_relaxed_u64(bar, ((uint64_t)kEpochMark << 32) | (e + 1u));
+            return;
+        }
+    }
+    if (tid == 0) TQ_PHASE(trace_slot, 8);
+    constexpr int kRowsPerWarp = kGridMergeMaxCtas / kConsumers;
+    const int SL = D / 32, R = n_splits;   // slices per head: (block, c) pairs
+    const int n_items = Hq * SL;
+    bool advanced = false;
+    for (int item = me; item < n_items; item += n_ctas) {
+        // slice sl: coordinates 4 lane + (sl & 3) of block sl >> 2, stored at words 32 sl + lane
+        const int sl = item % SL, hh = item / SL;
+        const uint64_t *base = reinterpret_cast<const uint64_t *>(part) + (int64_t)hh * PS;
+        // warp w sums rows w, w + kConsumers, ... (lane = coordinate); thread t < R
+        // brings row t's (m, l): every load of one reading is in flight at once
+        float ov[kRowsPerWarp];
+        float2 ml = make_float2(-INFINITY, 0.f);
+        bool done = false;
+        for (uint32_t it = 0; it < wait_limit && !done; ++it) {
+            bool mine = true;
+#pragma unroll
+            for (int k = 0; k < kRowsPerWarp; ++k) {
+                const int r = warp + kConsumers * k;
+                const uint64_t wv = r < R ? ld_relaxed_u64(base + r * rw + 32 * sl + lane)
+                                          : (uint64_t)tag << 32;
+                mine &= (uint32_t)(wv >> 32) == tag;
+                ov[k] = __uint_as_float((uint32_t)wv);
+            }
+            if (tid < R) {
+                const uint64_t wm = ld_relaxed_u64(base + tid * rw + D);
+                const uint64_t wl = ld_relaxed_u64(base + tid * rw + D + 1);
+                mine &= (uint32_t)(wm >> 32) == tag && (uint32_t)(wl >> 32) == tag;
+                ml = make_float2(__uint_as_float((uint32_t)wm), __uint_as_float((uint32_t)wl));
+            }
+            done = __syncthreads_and(mine) != 0;
+        }
+        if (!done) {
+            if (tid == 0) record_error(TQ_ERR_DEVICE_TIMEOUT);
+            break;
+        }
+        if (me == 0 && tid == 0 && !advanced) {
+            st_relaxed_u64(bar, ((uint64_t)kEpochMark << 32) | (e + 1u));
+            advanced = true;
+        }
+        if (tid == 0 && item == me) TQ_PHASE(trace_slot, 9);
+        float mx = ml.x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) s_red[warp] = mx;
+        __syncthreads();
+        float M = s_red[0];
+        for (int w = 1; w < kConsumers; ++w) M = fmaxf(M, s_red[w]);
+        const float wr = ml.x == -INFINITY ? 0.f : __expf(ml.x - M);
+        if (tid < R) s_w[tid] = wr;
+        float lw = wr * ml.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+        if (lane == 0) s_red[kConsumers + warp] = lw;
+        __syncthreads();
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < kRowsPerWarp; ++k) {
+            const int r = warp + kConsumers * k;
+            if (r < R) acc = fmaf(s_w[r], ov[k], acc);
+        }
+        s_acc[warp * 32 + lane] = acc;
+        __syncthreads();
+        if (warp == 0) {
+            float L = 0.f, o = 0.f;
+            for (int w = 0; w < kConsumers; ++w) {
+                L += s_red[kConsumers + w];
+                o += s_acc[w * 32 + lane];
+            }
+            const float inv = L > 0.f ? kInvSqrt128 / L : 0.f;
+            out[(int64_t)hh * D + kBlock * (sl >> 2) + 4 * lane + (sl & 3)] = o * inv;
+        }
+        __syncthreads();   // the scratch is reused by the next item
+    }
+    if (me == 0 && tid == 0 && !advanced) st_relaxed_u64(bar, ((uint64_t)kEpochMark << 32) | (e + 1u));
+    if (tid == 0) TQ_PHASE(trace_slot, 10);
 }
 
 // APPEND: the decode-step form (p.k_new set); a separate instantiation, so that the plain
@@ -203,6 +341,15 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     // so whatever the kernel before this one writes, the loads after the wait see it; the
     // prefetch only moves the DRAM latency of those first loads under that kernel's tail
     // (at a 32K context the length and query loads took about 2 us after the wait).
+    // Tile 0 holds TT / 2 tokens, the others TT: with every CTA requesting its first tile
+    // at once, a short first tile arrives sooner and the compute starts while the rest of
+    // the split streams in.
+    const int TF = TT / 2;
+    const int64_t t_begin = (int64_t)split * p.tokens_per_split;
+    // In a contiguous cache the first tile's rows are known before the length: their
+    // addresses are formed here, and the copy is requested right after the length load
+    // when the tile turns out full and free of the new row (every CTA but the last ones).
+    const uint8_t *pre_k = nullptr, *pre_v = nullptr;
     if (tid == 0) {
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p.seq_lens + seq));
         l2_prefetch(p.q + (int64_t)seq * Hq * D, (uint32_t)(Hq * D * 2));
@@ -210,36 +357,76 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             l2_prefetch(p.k_new + (int64_t)seq * Hkv * D, (uint32_t)(Hkv * D * 2));
             l2_prefetch(p.v_new + (int64_t)seq * Hkv * D, (uint32_t)(Hkv * D * 2));
         }
-        const int64_t t0 = (int64_t)split * p.tokens_per_split;
-        const int64_t t1 = min64(min64(t0 + TT / 2, t0 + p.tokens_per_split), p.max_len);
+        const int64_t t1 = min64(min64(t_begin + TF, t_begin + p.tokens_per_split), p.max_len);
         if (!p.kc.page_tokens && !p.vc.page_tokens && seq < p.kc.n_seqs && seq < p.vc.n_seqs) {
             const int64_t e = min64(t1, min64(p.kc.capacity, p.vc.capacity));
-            if (e > t0) {
-                l2_prefetch(p.kc.base + (seq * p.kc.capacity + t0) * (int64_t)Rk, (uint32_t)((e - t0) * Rk));
-                l2_prefetch(p.vc.base + (seq * p.vc.capacity + t0) * (int64_t)Rv, (uint32_t)((e - t0) * Rv));
+            if (e > t_begin) {
+                const uint8_t *k0 = p.kc.base + (seq * p.kc.capacity + t_begin) * (int64_t)Rk;
+                const uint8_t *v0 = p.vc.base + (seq * p.vc.capacity + t_begin) * (int64_t)Rv;
+                l2_prefetch(k0, (uint32_t)((e - t_begin) * Rk));
+                l2_prefetch(v0, (uint32_t)((e - t_begin) * Rv));
+                if (e == t_begin + TF) {
+                    pre_k = k0;
+                    pre_v = v0;
+                }
             }
         }
+        // this CTA's partial rows (written at the end): address translation warmed early
+        const int64_t grp = split / p.cl;
+        l2_prefetch(p.part + (seq * (p.n_splits / p.cl) + grp) * Hq * part_stride(D),
+                    (uint32_t)(Hq * part_stride(D) * sizeof(float)));
     }
+    // The fp16 codebook tables and the last parameters, from the constant cache: their first
+    // reads miss it, so they are made here, while the previous kernel runs (the codebook is
+    // written by host copies only, never by a kernel).
+    const HalfTables tk = make_tables<TK>(), tv = make_tables<TV>();
+    asm volatile("" ::"r"(tk.l0), "r"(tk.l1), "r"(tk.h0), "r"(tk.h1), "r"(tv.l0), "r"(tv.l1),
+                 "r"(tv.h0), "r"(tv.h1), "r"(p.mul2), "r"(p.hi31));
     // everything above touches only shared memory (and L2 prefetches); inputs may come from
     // the kernel launched before this one
     pdl_wait();
     pdl_launch_dependents();
     if (tid == 0) TQ_PHASE(trace_slot, 1);
 
+    // The query blocks of the rotation's first pass are requested first: the first tile's
+    // copies, which all CTAs request right after the length load, then fill the memory
+    // system for about a microsecond.
+    constexpr int kRot = kConsumers - 1;
+    uint2 qraw[5];
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int hb = warp - 1 + k * kRot;
+        const int h = hb / NB, b = hb - h * NB;
+        qraw[k] = warp > 0 && hb < Hq * NB
+                      ? *reinterpret_cast<const uint2 *>(p.q + ((int64_t)seq * Hq + h) * D + b * kBlock + 4 * lane)
+                      : make_uint2(0u, 0u);
+    }
+
+    // grid merge: the workspace's epoch word, read now by the last warp's lane 0 and parked
+    // in shared memory after the rotation (its L2 latency stays off the epilogue)
+    uint64_t epoch_word = 0;
+    if (p.out && tid == 32 * (kConsumers - 1)) epoch_word = ld_relaxed_u64(p.bar);
+
     int64_t len = p.seq_lens[seq];
     if (len < 0 || len > p.max_len) {
         if (tid == 0) record_error(TQ_ERR_OUT_OF_RANGE);
         len = len < 0 ? 0 : p.max_len;
     }
+    // the first tile is full (TF rows) and does not hold the new row (position len - 1)
+    const bool early0 = pre_k && len - (APPEND ? 1 : 0) >= t_begin + TF;
+    if (tid == 0 && early0 && !p.withhold_tiles) {
+        const uint32_t bar = smem_u32(&full[0]);
+        asm volatile("mbarrier.expect_tx.shared.b64 [%0], %1;\n" ::"r"(bar), "r"((uint32_t)TF * (uint32_t)(Rk + Rv))
+                     : "memory");
+        bulk_g2s(smem_u32(stage0), pre_k, (uint32_t)TF * (uint32_t)Rk, bar);
+        bulk_g2s(smem_u32(stage0 + (size_t)TT * Rk), pre_v, (uint32_t)TF * (uint32_t)Rv, bar);
+        asm volatile("mbarrier.arrive.shared.b64 _, [%0];\n" ::"r"(bar) : "memory");
+    }
     if (tid == 0) TQ_PHASE(trace_slot, 2);
-    const int64_t t_begin = (int64_t)split * p.tokens_per_split;
     const int64_t t_end = min64(len, t_begin + p.tokens_per_split);
-    // Tile 0 holds TT / 2 tokens, the others TT: with every CTA requesting its first tile
-    // at once, a short first tile arrives sooner and the compute starts while the rest of
-    // the split streams in.
-    const int TF = TT / 2;
-    const int64_t span = t_end - t_begin;
-    const int n_tiles = span <= 0 ? 0 : span <= TF ? 1 : 1 + (int)((span - TF + TT - 1) / TT);
+    // 32-bit from here: a split is at most tokens_per_split rows
+    const int span = (int)max64(t_end - t_begin, 0);
+    const int n_tiles = span == 0 ? 0 : span <= TF ? 1 : 1 + (span - TF + TT - 1) / TT;
     auto tile_start = [&](int i) -> int64_t { return t_begin + (i == 0 ? 0 : TF + (int64_t)(i - 1) * TT); };
     auto tile_len = [&](int i) -> int { return (int)min64(i == 0 ? TF : TT, t_end - tile_start(i)); };
     // ---- decode-step append (k_new set): the CTA whose split holds the new row (position
@@ -249,7 +436,7 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
     // straight into the stage and the tile's TMA copy stops one row short, so the new row
     // costs no round trip through memory.  Otherwise an async-proxy fence and the barrier
     // below order the stores before the refill that copies the row; no other CTA reads it.
-    const bool owner = APPEND && len > 0 && split == (int)((len - 1) / p.tokens_per_split);
+    const bool owner = APPEND && len > 0 && len - 1 >= t_begin && len - 1 < t_begin + p.tokens_per_split;
     const int i_new = owner ? n_tiles - 1 : -1;            // the tile holding the new row
     const bool new_in_stage = owner && i_new < p.stages;
     const int bpr = Hkv * NB;
@@ -269,25 +456,25 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         uint8_t *dk = stage0 + (size_t)(i % p.stages) * p.stage_bytes;
         issue_tile(p, seq, t0, nt, dk, dk + (size_t)TT * Rk, smem_u32(&full[i % p.stages]));
     };
-    if (tid == 0 && n_tiles > 0) issue(0);
+    if (tid == 0 && n_tiles > 0 && !early0) issue(0);
     if (tid == 0) TQ_PHASE(trace_slot, 3);
     if (warp == 0)   // the zero row of lanes without a head (warp 0 rotates nothing)
         for (int i = lane; i < QS / 8; i += 32)
             reinterpret_cast<uint4 *>(qh + 2 * Hq * QS)[i] = make_uint4(0u, 0u, 0u, 0u);
     // ---- rotate q once per call: y = W q_b * score_scale, stored as hi = fp16(y) and
-    // lo = fp16(y - hi), by warps 1-15; a warp loads its (up to five) query blocks at once,
-    // then rotates them
-    constexpr int kRot = kConsumers - 1;
+    // lo = fp16(y - hi), by warps 1-15; a warp loads its (up to five) query blocks at once
+    // (those of the first pass above), then rotates them
     if (warp > 0)
     for (int hb0 = warp - 1; hb0 < Hq * NB; hb0 += 5 * kRot) {
-        uint2 qraw[5];
+        if (hb0 != warp - 1) {
 #pragma unroll
-        for (int k = 0; k < 5; ++k) {
-            const int hb = hb0 + k * kRot;
-            const int h = hb / NB, b = hb - h * NB;
-            qraw[k] = hb < Hq * NB
-                          ? *reinterpret_cast<const uint2 *>(p.q + ((int64_t)seq * Hq + h) * D + b * kBlock + 4 * lane)
-                          : make_uint2(0u, 0u);
+            for (int k = 0; k < 5; ++k) {
+                const int hb = hb0 + k * kRot;
+                const int h = hb / NB, b = hb - h * NB;
+                qraw[k] = hb < Hq * NB
+                              ? *reinterpret_cast<const uint2 *>(p.q + ((int64_t)seq * Hq + h) * D + b * kBlock + 4 * lane)
+                              : make_uint2(0u, 0u);
+            }
         }
 #pragma unroll
         for (int k = 0; k < 5; ++k) {
@@ -337,8 +524,10 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         }
         if (!new_in_stage) asm volatile("fence.proxy.async.global;\n" ::: "memory");
     }
+    if (p.out && tid == 32 * (kConsumers - 1)) full[8] = epoch_word;   // past the barriers
     __syncthreads();
-    if (tid == 0) TQ_PHASE(trace_slot, 4);
+    // (a read of another warp's store keeps the stamp after the barrier)
+    if (tid == 0 && __half_as_ushort(qh[0]) != 0x7e01u) TQ_PHASE(trace_slot, 4);
 
     bool timed_out = false;
 
@@ -370,23 +559,6 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
         auto bq_lo = [&](int b, int j) -> uint2 {
             return *reinterpret_cast<const uint2 *>(qrow_lo + b * kBlock + 16 * j);
         };
-        HalfTables tk, tv;
-        {
-            const __half *ck = c_codebook[cb_index(TK)].centroid_h;
-            const __half *cv = c_codebook[cb_index(TV)].centroid_h;
-            uint32_t lk[2] = {0, 0}, hk[2] = {0, 0}, lv[2] = {0, 0}, hv[2] = {0, 0};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint16_t a = e < (1 << TK) ? __half_as_ushort(ck[e]) : 0;
-                const uint16_t c = e < (1 << TV) ? __half_as_ushort(cv[e]) : 0;
-                lk[e >> 2] |= (uint32_t)(a & 0xff) << (8 * (e & 3));
-                hk[e >> 2] |= (uint32_t)(a >> 8) << (8 * (e & 3));
-                lv[e >> 2] |= (uint32_t)(c & 0xff) << (8 * (e & 3));
-                hv[e >> 2] |= (uint32_t)(c >> 8) << (8 * (e & 3));
-            }
-            tk = {lk[0], lk[1], hk[0], hk[1]};
-            tv = {lv[0], lv[1], hv[0], hv[1]};
-        }
         // word alignment of this warp's blocks (same for every row: rows are 16-byte
         // multiples) and the word-aligned offsets of this lane's quarter within a row
         uint32_t shk[NB], shv[NB];
@@ -668,6 +840,49 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
             }
         }
     }
+    if (p.out) {
+        // ---------------- grid merge (one sequence whose splits run as one wave, launched
+        // cooperatively).  Each CTA writes its partial rows turned back from the rotated
+        // basis (o = D W o~; W is its own inverse up to 1/sqrt(128), applied with the
+        // normalisation) as 64-bit words (value, tag), the tag a hash of the epoch word at
+        // the start of the workspace.  The CTAs then merge the (head, 32-coordinate) slices
+        // assigned to them (coordinates 4 l + c, l = 0..31, of one block: one contiguous run
+        // of words), re-reading a slice until every word carries this call's tag: a
+        // word is written and read whole, so a matching tag means a current value, and no
+        // barrier is needed (words left by earlier calls carry other tags).  The first CTA
+        // advances the epoch once its slice is complete, that is once every CTA has read
+        // the epoch.  A workspace whose epoch word lacks kEpochMark (not yet used by this
+        // form: its words may hold anything) first passes a barrier of per-CTA flags with
+        // 64-bit tokens.
+        const uint64_t E = full[8];
+        const bool marked = (uint32_t)(E >> 32) == kEpochMark;
+        const uint32_t e = marked ? (uint32_t)E : 0u;
+        const uint32_t tag = (e + 1u) * 0x9E3779B9u;
+        const int64_t rw = (int64_t)Hq * PS;    // 64-bit words between consecutive splits' rows
+        uint64_t *prow = reinterpret_cast<uint64_t *>(p.part) + (int64_t)split * rw;
+        __syncthreads();   // cpart complete
+        for (int hb = warp; hb < Hq * NB; hb += kConsumers) {
+            const int h = hb / NB, b = hb - h * NB;
+            const float4 x = *reinterpret_cast<const float4 *>(cpart + h * PS + b * kBlock + 4 * lane);
+            float v[4] = {x.x, x.y, x.z, x.w};
+            warp_fwht4(v, lane);
+            apply_signs4(v, p.vc, 4 * lane);
+            // coordinate 4 lane + c of the block at word 32 c + lane: each store is one
+            // contiguous 256-byte run
+            uint64_t *dst = prow + (int64_t)h * PS + b * kBlock + lane;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) st_relaxed_u64(dst + 32 * c, tagged(v[c], tag));
+        }
+        for (int h = tid; h < Hq; h += 32 * kConsumers) {
+            st_relaxed_u64(prow + (int64_t)h * PS + D, tagged(cpart[h * PS + D], tag));
+            st_relaxed_u64(prow + (int64_t)h * PS + D + 1, tagged(cpart[h * PS + D + 1], tag));
+        }
+        __syncthreads();
+        if (tid == 0) TQ_PHASE(trace_slot, 7);
+        grid_merge<kConsumers>(p.part, p.bar, p.out, stage0, E, marked, e, tag, Hq, D, p.n_splits,
+                               p.grid_wait_limit, trace_slot);
+        return;
+    }
     // ---------------- the CTAs of a cluster (consecutive splits) merge their partials
     // through distributed shared memory: CTA rank r owns heads r, r + CL, ...  (a cluster of
     // one CTA writes its own partial rows)
@@ -752,6 +967,8 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
 
 template <int TK, int TV, int NB, bool APPEND, bool QLO2>
 tq_status launch_tt(const MmaParams &p, int n_seqs, cudaStream_t stream) {
+    static_assert(kGridMergeMaxCtas % (32 * 1) == 0 && kGridMergeMaxCtas <= 32 * consumers(NB),
+                  "one (m, l) load per thread in the grid merge");
     const size_t qbytes = q_bytes(p.n_q_heads, NB);
     const size_t smem = qbytes + 128 + (size_t)p.stages * p.stage_bytes;
     // the most any shape asks for, so the attribute is set once per device
@@ -760,10 +977,15 @@ tq_status launch_tt(const MmaParams &p, int n_seqs, cudaStream_t stream) {
                                       (int)kSmemBudget, 32 * consumers(NB), nullptr);
     if (st != TQ_OK) return st;
     PdlConfig lc(dim3(p.n_splits, n_seqs), dim3(32 * consumers(NB)), smem, stream);
-    lc.attrs[1].id = cudaLaunchAttributeClusterDimension;
-    lc.attrs[1].val.clusterDim.x = (unsigned)p.cl;
-    lc.attrs[1].val.clusterDim.y = 1;
-    lc.attrs[1].val.clusterDim.z = 1;
+    if (p.out) {   // the grid merge: every CTA resident at once (one per SM)
+        lc.attrs[1].id = cudaLaunchAttributeCooperative;
+        lc.attrs[1].val.cooperative = 1;
+    } else {
+        lc.attrs[1].id = cudaLaunchAttributeClusterDimension;
+        lc.attrs[1].val.clusterDim.x = (unsigned)p.cl;
+        lc.attrs[1].val.clusterDim.y = 1;
+        lc.attrs[1].val.clusterDim.z = 1;
+    }
     lc.cfg.numAttrs = 2;
     return check_cuda(cudaLaunchKernelEx(&lc.cfg, attn_mma_kernel<TK, TV, NB, APPEND, QLO2>, p));
 }
@@ -791,6 +1013,10 @@ size_t stage_bytes_for(int tile_tokens, size_t rk, size_t rv) {
 
 }  // namespace
 
+bool grid_merge_fits(int n_seqs, int n_splits) {
+    return n_seqs == 1 && n_splits <= std::min(device_sm_count(), kGridMergeMaxCtas);
+}
+
 bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
     const int hkv = k.n_kv_heads, nb = k.head_dim / kBlock, G = n_q_heads / hkv;
     if (nb < 1 || nb > 2 || G > 8) return false;
@@ -807,7 +1033,8 @@ bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
                           int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
                           float *part, int n_splits, int tokens_per_split, int cluster,
-                          const void *k_new, const void *v_new, cudaStream_t stream) {
+                          const void *k_new, const void *v_new, float *out, uint64_t *bar,
+                          cudaStream_t stream) {
     MmaParams p;
     p.kc = make_view(k);
     p.vc = make_view(v);
@@ -830,6 +1057,10 @@ tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, i
     p.tile_tokens = kWarpTokens * p.wph;
     p.wait_limit = kWaitLimit;
     p.withhold_tiles = 0;
+    p.out = out;
+    p.bar = bar;
+    p.grid_wait_limit = kGridWaitLimit;
+    if (out && (cluster != 1 || !bar || !grid_merge_fits(n_seqs, n_splits))) return TQ_ERR_UNSUPPORTED;
     for (int n = g_inject_timeouts.load(); n > 0;)
         if (g_inject_timeouts.compare_exchange_weak(n, n - 1)) {
             p.wait_limit = kInjectedWaitLimit;

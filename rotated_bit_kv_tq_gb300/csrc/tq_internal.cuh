@@ -24,6 +24,11 @@ __host__ __device__ constexpr int block_bytes(int type) { return 2 + kBlock * ty
 // with work to an empty one, which then holds its SM until its partner is done).
 constexpr int kClusterSplits = 2;
 
+// Decode workspace: the grid-merge area (an epoch word and one arrival flag per CTA of a
+// decode launch that merges its own partials after a grid barrier), then the partial rows.
+constexpr int kGridMergeMaxCtas = 160;   // one wave on 152 SMs; a multiple of 32, 16 and 8
+constexpr size_t kGridBarrierBytes = 4096;   // >= 8 * (1 + kGridMergeMaxCtas), 256-aligned
+
 // Floats per split-partial row of one (sequence, split, query head): head_dim rotated-domain
 // sums, the running max m, the running sum l, two pad floats (rows stay 16-byte aligned).
 __host__ __device__ constexpr int part_stride(int head_dim) { return head_dim + 4; }
@@ -111,6 +116,15 @@ __device__ __forceinline__ uint8_t *row_ptr(const CacheView &c, int64_t seq, int
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
+// Issued before pdl_wait() it is safe even for data the previous kernel still writes: it
+// fills nothing in the SM, and L2 is where device memory is coherent, so the loads after
+// the wait see the final contents; what it saves is the first access's latency (DRAM and
+// address translation), which otherwise falls after the wait.
+__device__ __forceinline__ void l2_prefetch(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ------------------------------------------------------------------ phase trace
@@ -214,11 +228,16 @@ tq_status launch_append(const tq_cache &k, const tq_cache &v, const void *k_new,
 // Tensor-core decode attention (tq_attn_mma.cu): writes split partials like the fp32 kernel.
 bool attn_mma_supported(const tq_cache &k, const tq_cache &v, int n_q_heads);
 // `cluster` consecutive splits (2 or 1) merge their partials in distributed shared memory;
-// the kernel writes n_splits / cluster partial rows per (sequence, head).
+// the kernel writes n_splits / cluster partial rows per (sequence, head).  With `out` set
+// (grid_merge_fits: one sequence, one wave; cluster 1) the CTAs merge the partials
+// themselves and write the output, no merge kernel following; `bar` is the grid-merge area
+// (its epoch word persists from call to call) and `part` holds tagged 64-bit words.
+bool grid_merge_fits(int n_seqs, int n_splits);
 tq_status launch_attn_mma(const tq_cache &k, const tq_cache &v, const void *q, int n_seqs,
                           int n_q_heads, const int32_t *seq_lens, int64_t max_seq_len, float scale,
                           float *part, int n_splits, int tokens_per_split, int cluster,
-                          const void *k_new, const void *v_new, cudaStream_t stream);
+                          const void *k_new, const void *v_new, float *out, uint64_t *bar,
+                          cudaStream_t stream);
 
 // Fault injection of tq_inject_wait_timeout (tq_attn_mma.cu).
 tq_status inject_wait_timeout(int n_calls);

@@ -302,6 +302,48 @@ def test_attn_equal_keys_give_mean(tq):
     assert_attn_close(got, ref, "decode equal keys")
 
 
+def test_grid_merge_epochs_on_a_reused_workspace(tq):
+    """Decode calls that merge their own partials after a grid barrier (one wave of CTAs),
+    all on one workspace whose barrier area starts as random bytes.  The calls alternate
+    between grids of different sizes, a batch that takes the merge kernel instead, and a
+    repeat of the first shape.  Each call gets a new query, so a barrier passed on an
+    earlier call's flags would merge stale partials.  Every output must equal, bit for
+    bit, that of the same call on a fresh zeroed workspace, and each matches the oracle."""
+    w = synth.LLAMA3_8B_32K
+    Hkv, Hq, D = w.n_kv_heads, w.n_q_heads, w.head_dim
+    S = 3
+    cap = 5100   # 3 sequences of 5,100 tokens: 3 x 51 splits, more CTAs than one wave
+    kc = tq.KVCache(3, Hkv, D, n_seqs=S, capacity_tokens=cap)
+    vc = tq.KVCache(3, Hkv, D, n_seqs=S, capacity_tokens=cap)
+    ks = [_kv(w, 2, "K", cap, seq=s) for s in range(S)]
+    vs = [_kv(w, 2, "V", cap, seq=s) for s in range(S)]
+    for s in range(S):
+        tq.encode(kc, torch.from_numpy(ks[s]).to(DEV), seq_id=s)
+        tq.encode(vc, torch.from_numpy(vs[s]).to(DEV), seq_id=s)
+    calls = [(1, 1500), (1, 333), (S, cap), (1, 1500), (1, 40), (1, cap)]
+    ws_bytes = max(tq.attn_workspace_bytes(n, Hq, D, L) for n, L in calls)
+    shared = torch.randint(0, 256, (ws_bytes,), dtype=torch.uint8,
+                           generator=torch.Generator().manual_seed(11)).to(DEV)
+    for i, (n, L) in enumerate(calls):
+        q16 = np.stack([synth.query(w, 2, 10 + i, s) for s in range(n)])
+        q = torch.from_numpy(q16).to(DEV)
+        lens = torch.full((n,), L, dtype=torch.int32, device=DEV)
+        fresh = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
+        want = torch.empty(n, Hq, D, device=DEV)
+        got = torch.empty(n, Hq, D, device=DEV)
+        tq.attn_decode(kc, vc, q, lens, L, want, fresh)
+        tq.attn_decode(kc, vc, q, lens, L, got, shared)
+        torch.cuda.synchronize()
+        assert tq.device_status() == 0
+        assert torch.equal(got, want), f"call {i} ({n} x {L}) differs on the reused workspace"
+        o = got.cpu().numpy().astype(np.float64)
+        for s in range(n):
+            kr = oracle.encode_rows(3, ks[s][:L], Hkv, D)
+            vr = oracle.encode_rows(3, vs[s][:L], Hkv, D)
+            ref = oracle.attn_decode(3, 3, kr, vr, q16[s], L, Hq, Hkv, D, 1.0 / np.sqrt(D))
+            assert_attn_close(o[s], ref, f"grid merge call {i} s{s} L{L}")
+
+
 def test_attn_workspace_too_small_is_rejected(tq):
     kc = tq.KVCache(3, 2, 128, capacity_tokens=64)
     q = torch.zeros(1, 4, 128, dtype=torch.float16, device=DEV)
