@@ -181,6 +181,17 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&r)[32]) {
         : "memory");
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+          "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+          "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 // 64 consecutive fp32 columns of this thread's TMEM lane (two loads, one wait, in one
 // statement so that no use of the values can be scheduled before the wait).
 __device__ __forceinline__ void tc_ld64(uint32_t taddr, float (&r)[64]) {
@@ -742,6 +753,401 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
+// ------------------------------------------------------------------ head_dim 256
+// Two 128-value blocks per head, each rotated and quantised on its own, each with its own
+// norm.  The scores need both blocks of the query and of every key; the query's high and
+// low fp16 parts over 256 coordinates (128 KB for 128 rows) then no longer fit in shared
+// memory beside the operand tiles, so they live in tensor memory as the A operand of the
+// score MMAs, and P moves to shared memory as the A operand of P V.  A key tile holds 64
+// keys, and the two blocks' products go to separate halves of the score buffer
+// (S_b = Q~_b C_b^T, N = 64 each), so each block is scaled by its own norm in fp32, as at
+// head_dim 128.  Each CTA produces one 128-coordinate block of the output (two CTAs per
+// query block, both computing the scores).
+// Tensor memory columns: S [0,128) (block 0 keys, then block 1 keys), O [128,256),
+// Q~ high [256,384), Q~ low [384,512).
+constexpr int k2Keys = 64;   // keys per tile
+constexpr uint32_t k2S = 0, k2O = 128, k2Qh = 256, k2Ql = 384;
+
+enum {
+    k2BarQ = 0,        // queries written (256 arrivals)
+    k2BarKFull = 1,    // [2] K tile (both blocks) and norms decoded (128 arrivals)
+    k2BarKFree = 3,    // [2] the tile's score MMAs done: K buffer free (commit)
+    k2BarSFull = 5,    // scores ready (commit)
+    k2BarSFree = 6,    // scores and norms read (256 arrivals)
+    k2BarVFull = 7,    // [2] V tile decoded (64 arrivals)
+    k2BarPFull = 9,    // [2] P written, O rescaled (256 arrivals)
+    k2BarPvFree = 11,  // [2] the tile's P V done: V tile and P buffer free (commit)
+    k2BarDrain = 13,   // every MMA of the CTA done (commit)
+    k2BarCount = 14
+};
+
+struct TcSmem256 {
+    alignas(1024) uint8_t k[2][2][16384];  // [buffer][block] K tile [key][coord], K-major
+    alignas(1024) uint8_t v[2][16384];     // [buffer] V tile of the output block, MN-major
+    alignas(1024) uint8_t p[2][16384];     // [buffer] P [row][key] fp16, K-major
+    alignas(1024) uint8_t xo[65536];       // epilogue: the two halves of every output row
+    alignas(16) uint8_t raw_k[2][kTcKeys * 64];   // staged K blocks (word-major, stride kTcKeys)
+    alignas(16) uint8_t raw_v[kTcKeys * 64];
+    // [tile mod 3][block][key] norms: the producer writes tile i + 2's norms once tile i's
+    // score MMAs are done, possibly before the softmax has read tile i's
+    float kn[3][2][k2Keys];
+    float xch[2][2][kTcRows];
+    uint8_t ok[3][kTcKeys];                // K block 0, K block 1, V: key present
+    alignas(8) uint64_t bar[k2BarCount];
+    uint32_t tmem;
+};
+
+// Element (row, key) of a 64-key K-major tile: 8 core matrices along K, so 8-row groups sit
+// 1024 bytes apart.
+__device__ __forceinline__ uint32_t canon64(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B (both K-major), M = 128,
+// N = 64.
+constexpr uint32_t idesc_f16_n64() {
+    return (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+template <int TK, int TV>
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    TcSmem256 &sm = *reinterpret_cast<TcSmem256 *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // CTA 2 q + ob produces output block ob of query CTA q (longest first, as above)
+    const int ob = (int)(blockIdx.x & 1u);
+    const unsigned qcta = blockIdx.x >> 1;
+    const int g = (int)(qcta % (unsigned)p.n_kv_heads), G = p.group, Hq = p.n_q_heads;
+    const int64_t j0 = (p.n_qblocks - 1 - (int64_t)(qcta / (unsigned)p.n_kv_heads)) * p.bq;
+    const int64_t j_end = min64(p.n_q, j0 + p.bq);
+    const int64_t n_keys = p.pos0 + j_end;
+    const int64_t first_pos = p.pos0 + j0;
+    const int n_tiles = (int)((n_keys + k2Keys - 1) / k2Keys);
+    constexpr int D = 2 * kBlock;
+    auto bar = [&](int i) { return smem_u32(&sm.bar[i]); };
+
+    if (tid == 0) {
+        abort_flag = 0;
+        tc_bar_init(bar(k2BarQ), kTcSoftmax);
+        tc_bar_init(bar(k2BarSFull), 1);
+        tc_bar_init(bar(k2BarSFree), kTcSoftmax);
+        for (int b = 0; b < 2; ++b) {
+            tc_bar_init(bar(k2BarKFull + b), kTcGroup);
+            tc_bar_init(bar(k2BarKFree + b), 1);
+            tc_bar_init(bar(k2BarVFull + b), k2Keys);
+            tc_bar_init(bar(k2BarPFull + b), kTcSoftmax);
+            tc_bar_init(bar(k2BarPvFree + b), 1);
+        }
+        tc_bar_init(bar(k2BarDrain), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&sm.tmem)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+    volatile int *abort_v = &abort_flag;
+
+    if (warp < kTcSoftmax / 32) {
+        // ================= softmax: thread (r, h) owns keys 32 h .. 32 h + 31 of every tile
+        const int quad = warp & 3, h = warp >> 2;
+        const int r = 32 * quad + lane, jl = r / G, hl = r - jl * G;
+        const bool valid = jl < p.bq && j0 + jl < p.n_q;
+        const int64_t qpos = valid ? p.pos0 + j0 + jl : INT64_MAX;
+        const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+        const uint32_t pair_bar = 3u + (uint32_t)quad;
+        // the query, block by block: coords 64 h .. 64 h + 63 of Q~_b = H (D q_b) * scale,
+        // hi and lo fp16 parts into tensor memory (two K values per column)
+#pragma unroll 1
+        for (int blk = 0; blk < 2; ++blk) {
+            float x[64];
+            if (valid) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    p.q + ((j0 + jl) * Hq + g * G + hl) * (int64_t)D + kBlock * blk);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 ua = src[c], ub = src[c + 8];
+                    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = 8 * c + 2 * e;
+                        const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&wa[e]));
+                        const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&wb[e]));
+                        float a0 = fa.x, a1 = fa.y, b0 = fb.x, b1 = fb.y;
+                        if (p.kc.has_signs) {
+                            a0 = __uint_as_float(__float_as_uint(a0) ^ sign_mask(p.kc, i0));
+                            a1 = __uint_as_float(__float_as_uint(a1) ^ sign_mask(p.kc, i0 + 1));
+                            b0 = __uint_as_float(__float_as_uint(b0) ^ sign_mask(p.kc, 64 + i0));
+                            b1 = __uint_as_float(__float_as_uint(b1) ^ sign_mask(p.kc, 64 + i0 + 1));
+                        }
+                        x[i0] = h ? a0 - b0 : a0 + b0;
+                        x[i0 + 1] = h ? a1 - b1 : a1 + b1;
+                    }
+                }
+                fwht64(x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) x[i] = 0.f;
+            }
+            // 16 columns (32 coords) at a time keeps the live registers down
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t w[16], wl[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    split_half2(x[32 * c + 2 * e] * p.score_scale, x[32 * c + 2 * e + 1] * p.score_scale,
+                                w[e], wl[e]);
+                tc_st16(tmem + lane_base + k2Qh + 64u * blk + 32u * h + 16u * c, w);
+                tc_st16(tmem + lane_base + k2Ql + 64u * blk + 32u * h + 16u * c, wl);
+            }
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        tc_arrive(bar(k2BarQ));
+
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int b = i & 1;
+            if (!*abort_v && !tc_wait(bar(k2BarSFull), (uint32_t)(i & 1))) *abort_v = 1;
+            tc_fence_after();
+            float s[32], s1[32];
+            tc_ld32(tmem + lane_base + k2S + 32u * h, s);
+            tc_ld32(tmem + lane_base + k2S + 64u + 32u * h, s1);
+            const float *n0 = sm.kn[i % 3][0] + 32 * h, *n1 = sm.kn[i % 3][1] + 32 * h;
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = m_run;
+            if ((int64_t)i * k2Keys + (k2Keys - 1) <= first_pos) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    s[j] = s[j] * n0[j] + s1[j] * n1[j];
+                    mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
+                }
+            } else {
+                const int64_t t0 = (int64_t)i * k2Keys + 32 * h;
+                const int lim = (int)max64(-1, min64(qpos - t0, 32));   // keys j > lim are masked
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    s[j] = j > lim ? -INFINITY : s[j] * n0[j] + s1[j] * n1[j];
+                    mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
+                }
+            }
+            // the score buffer and this tile's norms are free
+            tc_fence_before();
+            tc_arrive(bar(k2BarSFree));
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            sm.xch[b][h][r] = mx;
+            named_sync(pair_bar, 64);
+            mx = fmaxf(mx, sm.xch[b][h ^ 1][r]);
+            float alpha = 1.f;
+            if (m_run == -INFINITY || mx > m_run + 8.f) {
+                alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mx);
+                m_run = mx;
+            }
+            // P buffer b is free once tile i - 2's P V is done
+            if (i >= 2 && !*abort_v && !tc_wait(bar(k2BarPvFree + b), (uint32_t)(((i - 2) >> 1) & 1)))
+                *abort_v = 1;
+            tc_fence_after();
+            float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float mref = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {   // keys 32 h + 8 c .. + 7 of row r
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 8 * c + 2 * e;
+                    const float p0 = ex2(s[j] - mref), p1 = ex2(s[j + 1] - mref);
+                    ps8[j & 7] += p0;
+                    ps8[(j + 1) & 7] += p1;
+                    w[e] = pack_half2(p0, p1);
+                }
+                *reinterpret_cast<uint4 *>(sm.p[b] + canon64(r, 32 * h + 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+            l_run = l_run * alpha + psum;
+            if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                if (!*abort_v && !tc_wait(bar(k2BarPvFree + ((i - 1) & 1)), (uint32_t)(((i - 1) >> 1) & 1)))
+                    *abort_v = 1;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float t[32];
+                    tc_ld32(tmem + lane_base + k2O + 64u * h + 32u * c, t);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) t[e] *= alpha;
+                    tc_st32(tmem + lane_base + k2O + 64u * h + 32u * c, t);
+                }
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P for the MMA
+            tc_fence_before();
+            tc_arrive(bar(k2BarPFull + b));
+        }
+        // ---- epilogue: O / l for output block ob, inverse rotation, V signs, store
+        const bool done = n_tiles > 0 && !*abort_v &&
+                          tc_wait(bar(k2BarPvFree + ((n_tiles - 1) & 1)), (uint32_t)(((n_tiles - 1) >> 1) & 1));
+        tc_fence_after();
+        sm.xch[n_tiles & 1][h][r] = l_run;
+        float o[64];
+        if (n_tiles > 0) {
+            tc_ld64(tmem + lane_base + k2O + 64u * h, o);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) o[e] = 0.f;
+        }
+        fwht64(o);
+        float *xo = reinterpret_cast<float *>(sm.xo);
+        auto xo_at = [&](int row, int c4) { return xo + row * 128 + (((c4 ^ row) & 31) << 2); };
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            *reinterpret_cast<float4 *>(xo_at(r, 16 * h + c)) =
+                make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        named_sync(pair_bar, 64);
+        const float l_row = l_run + sm.xch[n_tiles & 1][h ^ 1][r];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const float4 u = *reinterpret_cast<const float4 *>(xo_at(r, 16 * (h ^ 1) + c));
+            const float pv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[4 * c + e] = h ? pv[e] - o[4 * c + e] : o[4 * c + e] + pv[e];
+        }
+        if (valid && done) {
+            const float inv = l_row > 0.f ? p.out_scale / l_row : 0.f;
+            float4 *dst = reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)D +
+                                                     kBlock * ob + 64 * h);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                float v4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v4[e] = __uint_as_float(__float_as_uint(o[4 * c + e] * inv) ^ sign_mask(p.vc, 64 * h + 4 * c + e));
+                dst[c] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+            }
+        }
+    } else if (warp < kTcMmaWarp) {
+        const int pt = (tid - kTcSoftmax) & (kTcGroup - 1);
+        const int key = pt & (k2Keys - 1);
+        if (tid - kTcSoftmax < kTcGroup) {
+            // ================= K producers: thread (block, key), double-buffered
+            const int blk = pt >> 6;
+            const HalfTables tab = make_tables<TK>();
+            if (n_tiles > 0) tc_stage<TK>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk, 0, n_keys, key);
+            cp_async_commit();
+            for (int i = 0; i < n_tiles; ++i) {
+                const int b = i & 1;
+                cp_async_wait<0>();
+                if (i >= 2 && !*abort_v && !tc_wait(bar(k2BarKFree + b), (uint32_t)(((i - 2) >> 1) & 1)))
+                    *abort_v = 1;
+                tc_decode<TK, false>(sm.raw_k[blk], sm.ok[blk], 2 * g + blk, tab, sm.k[b][blk], sm.kn[i % 3][blk], key);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc_arrive(bar(k2BarKFull + b));
+                if (i + 1 < n_tiles)
+                    tc_stage<TK>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk,
+                                 (int64_t)(i + 1) * k2Keys, n_keys, key);
+                cp_async_commit();
+            }
+            cp_async_wait<0>();
+        } else if (pt < k2Keys) {
+            // ================= V producers: the output block of every key, double-buffered
+            const HalfTables tab = make_tables<TV>();
+            if (n_tiles > 0) tc_stage<TV>(p.vc, p.seq, p.chunked_v, sm.raw_v, sm.ok[2], 2 * g + ob, 0, n_keys, key);
+            cp_async_commit();
+            for (int i = 0; i < n_tiles; ++i) {
+                const int b = i & 1;
+                cp_async_wait<0>();
+                if (i >= 2 && !*abort_v &&
+                    !tc_wait(bar(k2BarPvFree + b), (uint32_t)(((i - 2) >> 1) & 1)))
+                    *abort_v = 1;
+                tc_decode<TV, true>(sm.raw_v, sm.ok[2], 2 * g + ob, tab, sm.v[b], nullptr, key);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc_arrive(bar(k2BarVFull + b));
+                if (i + 1 < n_tiles)
+                    tc_stage<TV>(p.vc, p.seq, p.chunked_v, sm.raw_v, sm.ok[2], 2 * g + ob,
+                                 (int64_t)(i + 1) * k2Keys, n_keys, key);
+                cp_async_commit();
+            }
+            cp_async_wait<0>();
+        }
+    } else if (lane == 0) {
+        // ================= MMA issue (one thread)
+        constexpr uint32_t idesc_s = idesc_f16_n64(), idesc_pv = idesc_f16(true);
+        bool ok = tc_wait(bar(k2BarQ), 0);
+        int ns = 0, npv = 0;
+        uint32_t idle = 0;
+        while (ok && npv < n_tiles) {
+            bool progressed = false;
+            // S(ns) overwrites the single score buffer: the softmax has read S(ns - 1)
+            if (ns < n_tiles && tc_test(bar(k2BarKFull + (ns & 1)), (uint32_t)((ns >> 1) & 1)) &&
+                (ns == 0 || tc_test(bar(k2BarSFree), (uint32_t)((ns - 1) & 1)))) {
+                tc_fence_after();
+                // S_b = Q~_b C_b^T: A = Q~ block b from tensor memory (16 coords = 8 columns per
+                // MMA), B = the block's K tile; high parts, then low parts
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    const uint32_t k_base = smem_u32(sm.k[ns & 1][blk]);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc_mma_ts(tmem + k2S + 64u * blk, tmem + k2Qh + 64u * blk + 8u * kk,
+                                  sdesc(k_base + 256u * kk, 128, 2048), idesc_s, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc_mma_ts(tmem + k2S + 64u * blk, tmem + k2Ql + 64u * blk + 8u * kk,
+                                  sdesc(k_base + 256u * kk, 128, 2048), idesc_s, 1u);
+                }
+                tc_commit(bar(k2BarSFull));
+                tc_commit(bar(k2BarKFree + (ns & 1)));
+                ++ns;
+                progressed = true;
+            }
+            if (npv < ns && tc_test(bar(k2BarPFull + (npv & 1)), (uint32_t)((npv >> 1) & 1)) &&
+                tc_test(bar(k2BarVFull + (npv & 1)), (uint32_t)((npv >> 1) & 1))) {
+                tc_fence_after();
+                const int b = npv & 1;
+                const uint32_t p_base = smem_u32(sm.p[b]), v_base = smem_u32(sm.v[b]);
+                // A = P from shared memory (16 keys per MMA), B = the V tile
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma(tmem + k2O, sdesc(p_base + 256u * kk, 128, 1024),
+                           sdesc(v_base + 4096u * kk, 2048, 128), idesc_pv, (npv > 0 || kk > 0));
+                tc_commit(bar(k2BarPvFree + b));
+                ++npv;
+                progressed = true;
+            }
+            if (progressed) idle = 0;
+            else if (++idle > kTcPollLimit || *abort_v) {
+                if (!*abort_v) record_error(TQ_ERR_DEVICE_TIMEOUT);
+                ok = false;
+            }
+        }
+        if (!ok) *abort_v = 1;
+        tc_commit(bar(k2BarDrain));
+        tc_wait(bar(k2BarDrain), 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kTcMmaWarp)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+template <int TK, int TV>
+tq_status launch_tc256_t(const TcParams &p, unsigned n_ctas, cudaStream_t stream) {
+    static_assert(sizeof(TcSmem256) + 1024 <= 227 * 1024, "one CTA per SM");
+    const size_t smem = sizeof(TcSmem256) + 1024;
+    const tq_status st = kernel_setup(reinterpret_cast<const void *>(prefill_tc256_kernel<TK, TV>),
+                                      (int)smem, kTcThreads, nullptr);
+    if (st != TQ_OK) return st;
+    PdlConfig lc(dim3(2 * n_ctas), dim3(kTcThreads), smem, stream);
+    return check_cuda(cudaLaunchKernelEx(&lc.cfg, prefill_tc256_kernel<TK, TV>, p));
+}
+
 template <int TK, int TV>
 tq_status launch_tc_t(const TcParams &p, unsigned n_ctas, cudaStream_t stream) {
     const size_t smem = sizeof(TcSmem) + 1024;   // room to align the tiles to 1024 bytes
@@ -762,7 +1168,7 @@ tq_status launch_tc_t(const TcParams &p, unsigned n_ctas, cudaStream_t stream) {
 }  // namespace
 
 bool prefill_supported(const tq_cache &k, const tq_cache &v, int n_q_heads) {
-    if (k.head_dim != kBlock || v.head_dim != kBlock) return false;
+    if (k.head_dim != v.head_dim || (k.head_dim != kBlock && k.head_dim != 2 * kBlock)) return false;
     return n_q_heads % k.n_kv_heads == 0 && n_q_heads / k.n_kv_heads <= kTcRows;
 }
 
@@ -793,6 +1199,13 @@ tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, in
     const int64_t n_ctas = p.n_qblocks * k.n_kv_heads;
     if (n_ctas > 0x3fffffff) return TQ_ERR_UNSUPPORTED;
     const unsigned nc = (unsigned)n_ctas;
+    if (k.head_dim == 2 * kBlock) {   // two CTAs (output blocks) per query block, no key split
+        p.split = 1;
+        if (k.type == TQ_TURBO3 && v.type == TQ_TURBO3) return launch_tc256_t<3, 3>(p, nc, stream);
+        if (k.type == TQ_TURBO2 && v.type == TQ_TURBO2) return launch_tc256_t<2, 2>(p, nc, stream);
+        if (k.type == TQ_TURBO3 && v.type == TQ_TURBO2) return launch_tc256_t<3, 2>(p, nc, stream);
+        return launch_tc256_t<2, 3>(p, nc, stream);
+    }
     // Split each query block's key tiles over a cluster of two CTAs when that fills the last
     // wave of one-CTA-per-SM launches markedly better (the two CTAs both rotate the queries,
     // so a split costs a little): e.g. the 512 CTAs of a 2,048-token chunk of a Llama-shape

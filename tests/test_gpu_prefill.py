@@ -105,10 +105,10 @@ def test_prefill_zero_queries_and_unsupported_shapes(tq):
     kc = tq.KVCache(3, 2, 128, capacity_tokens=8)
     out = torch.empty((0, 4, 128), device=DEV)
     tq.attn_prefill(kc, kc, torch.zeros((0, 4, 128), dtype=torch.float16, device=DEV), out, pos0=3)
-    k256 = tq.KVCache(3, 2, 256, capacity_tokens=8)
+    k384 = tq.KVCache(3, 2, 384, capacity_tokens=8)   # three blocks per head: not taken
     with pytest.raises(tq.TQError) as e:
-        tq.attn_prefill(k256, k256, torch.zeros((2, 4, 256), dtype=torch.float16, device=DEV),
-                        torch.empty((2, 4, 256), device=DEV), pos0=0)
+        tq.attn_prefill(k384, k384, torch.zeros((2, 4, 384), dtype=torch.float16, device=DEV),
+                        torch.empty((2, 4, 384), device=DEV), pos0=0)
     assert e.value.status == 2
     with pytest.raises(tq.TQError) as e:   # a sequence the cache does not have
         tq.attn_prefill(kc, kc, torch.zeros((2, 4, 128), dtype=torch.float16, device=DEV),
@@ -139,6 +139,64 @@ def test_prefill_full_size_llama_chunk_sampled(tq):
     for j in (0, 1, 257, n_q - 1):
         ref = oracle.attn_decode(3, 3, kr, vr, q[j], pos0 + j + 1, 32, 8, 128, 1 / np.sqrt(128))
         _check(got[j][None], ref[None], f"prefill llama3-8b 32K last chunk#{j}")
+
+
+PREFILL256_CASES = [
+    # (tk, tv, n_kv_heads, n_q_heads, pos0, n_q) at head_dim 256 (two 128-value blocks per
+    # head; the K blocks of a key have different norms)
+    (2, 2, 4, 16, 100, 70),    # the head_dim-256 workload's heads (G 4), ragged last block
+    (3, 3, 2, 10, 0, 60),      # G 5; the first query sees one key
+    (3, 2, 1, 8, 300, 33),     # G 8, mixed types, 3 key tiles
+    (2, 3, 2, 2, 37, 150),     # G 1: 128 queries per CTA
+]
+
+
+@pytest.mark.parametrize("tk,tv,hkv,hq,pos0,n_q", PREFILL256_CASES)
+def test_prefill_head_dim_256_matches_oracle(tq, tk, tv, hkv, hq, pos0, n_q):
+    w = synth.scaled(synth.HD256_128K, n_kv_heads=hkv, n_q_heads=hq, ctx=pos0 + n_q)
+    n_rows = pos0 + n_q
+    k = synth.kv_tokens(w, 0, "K", 0, n_rows).reshape(n_rows, -1)
+    v = synth.kv_tokens(w, 0, "V", 0, n_rows).reshape(n_rows, -1)
+    kc = tq.KVCache(tk, hkv, 256, capacity_tokens=n_rows + 3)
+    vc = tq.KVCache(tv, hkv, 256, capacity_tokens=n_rows + 3)
+    tq.encode(kc, torch.from_numpy(k).to(DEV))
+    tq.encode(vc, torch.from_numpy(v).to(DEV))
+    q = _queries(w, 0, pos0, n_q)
+    out = torch.full((n_q, hq, 256), float("nan"), device=DEV)
+    tq.attn_prefill(kc, vc, torch.from_numpy(q).to(DEV), out, pos0=pos0)
+    assert tq.device_status() == 0
+    kr = kc.buffer[: n_rows * kc.row_bytes].cpu().numpy().reshape(n_rows, -1)
+    vr = vc.buffer[: n_rows * vc.row_bytes].cpu().numpy().reshape(n_rows, -1)
+    ref = oracle.attn_prefill(tk, tv, kr, vr, q, pos0, hkv, 256, 1 / np.sqrt(256))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    _check(got, ref, f"prefill hd256 turbo{tk}/{tv} Hkv{hkv} Hq{hq}#{pos0}+{n_q}")
+
+
+@pytest.mark.slow
+def test_prefill_full_size_head_dim_256_chunk_sampled(tq):
+    """The last 512-token chunk of the head_dim-256 workload's 131,072-token prompt (turbo2,
+    4 KV heads, 16 query heads): every query runs, and three sampled queries match the
+    oracle's decode step at their positions."""
+    w = synth.HD256_128K
+    T, n_q = w.ctx, 512
+    pos0 = T - n_q
+    k = synth.kv_tokens(w, 2, "K", 0, T).reshape(T, -1)
+    v = synth.kv_tokens(w, 2, "V", 0, T).reshape(T, -1)
+    kc = tq.KVCache(2, 4, 256, capacity_tokens=T)
+    vc = tq.KVCache(2, 4, 256, capacity_tokens=T)
+    tq.encode_kv(kc, vc, torch.from_numpy(k).to(DEV), torch.from_numpy(v).to(DEV))
+    q = _queries(w, 2, pos0, n_q)
+    out = torch.empty((n_q, 16, 256), device=DEV)
+    tq.attn_prefill(kc, vc, torch.from_numpy(q).to(DEV), out, pos0=pos0)
+    assert tq.device_status() == 0
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    kr = kc.buffer.cpu().numpy().reshape(T, -1)
+    vr = vc.buffer.cpu().numpy().reshape(T, -1)
+    for j in (0, 300, n_q - 1):
+        ref = oracle.attn_decode(2, 2, kr, vr, q[j], pos0 + j + 1, 16, 4, 256, 1 / np.sqrt(256))
+        _check(got[j][None], ref[None], f"prefill hd256 131K last chunk#{j}")
 
 
 SPLIT_CASES = [
