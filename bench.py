@@ -18,8 +18,8 @@ Workloads (--workload; the default is the headline, the Llama-3-8B-shaped 32K ca
   batched-paged-64seq  64 sequences of 1,024 .. 16,384 tokens in 256-token pages, turbo3;
                        every iteration appends and attends for all 64 sequences in one call
   --all runs these four, one JSON line each (two for the Qwen shape).
-Outside the timed step, the head_dim-128 single-sequence workloads also time prompt-chunk
-attention (tq_attn_prefill) on the last 2,048-token chunk of the prompt in every layer.
+Outside the timed step, the single-sequence workloads also time prompt-chunk attention
+(tq_attn_prefill) on the last 2,048-token chunk of the prompt in every layer.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME | --all]
@@ -61,7 +61,7 @@ TRAFFIC = {
     # context), "encode": DRAM bytes of one tq_encode_kv launch of one layer's prefill}
     # Llama-3-8B shape, turbo3: `--kernel-probe 32768` captures of the decode-step and encode
     # kernels under ncu; the encode capture is the benchmark's own launch size.
-    ("llama3-8b-kv-32k", 3): {"attn_per_token": 26323456 / 32768, "encode": 134294528 + 10227968},
+    ("llama3-8b-kv-32k", 3): {"attn_per_token": 26493696 / 32768, "encode": 134294528 + 10227968},
 }
 
 
@@ -421,9 +421,9 @@ def run_ours(args, w, tt, rank, world, local_rank, dist, cpu_baseline_on):
     final_ctx = lens0 + S                    # contexts of the timed launch (new row included)
 
     # prompt-chunk attention (tensor-bound, timed alone): the last PREFILL_CHUNK queries of
-    # the prompt over every layer's cache (single-sequence head_dim-128 workloads)
+    # the prompt over every layer's cache (single-sequence workloads)
     prefill_line = None
-    if not inp.batched and D == 128:
+    if not inp.batched:
         T = w.ctx
         pf_pos0 = T - PREFILL_CHUNK
         gen = torch.Generator(device=dev)

@@ -371,10 +371,6 @@ __global__ void __launch_bounds__(32 * consumers(NB), 1) attn_mma_kernel(const M
                 }
             }
         }
-        // this CTA's partial rows (written at the end): address translation warmed early
-        const int64_t grp = split / p.cl;
-        l2_prefetch(p.part + (seq * (p.n_splits / p.cl) + grp) * Hq * part_stride(D),
-                    (uint32_t)(Hq * part_stride(D) * sizeof(float)));
     }
     // The fp16 codebook tables and the last parameters, from the constant cache: their first
     // reads miss it, so they are made here, while the previous kernel runs (the codebook is
