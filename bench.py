@@ -338,15 +338,20 @@ def run_ours(args, w, tt, rank, world, local_rank, dist, cpu_baseline_on):
         lens_dev.copy_(lens_start)
         step_dev.zero_()
 
-    def attend_layer(l, nb, qb):
-        tq.attn_decode_append(kc[l], vc[l], nb[0, l, 0].view(n, Hkv, D), nb[0, l, 1].view(n, Hkv, D),
-                              qb[0, l], lens_dev, max_len, out_dev[l], ws)
+    # every layer's argument views into the iteration buffers, made once: a caller keeps its
+    # per-layer tensors, and slicing them anew per call would time PyTorch, not this library
+    layer_args = [(kc[l], vc[l], new_buf[0, l, 0].view(n, Hkv, D), new_buf[0, l, 1].view(n, Hkv, D),
+                   q_buf[0, l], out_dev[l]) for l in range(L)]
+
+    def attend_layer(l):
+        k_c, v_c, k_new, v_new, q_l, out_l = layer_args[l]
+        tq.attn_decode_append(k_c, v_c, k_new, v_new, q_l, lens_dev, max_len, out_l, ws)
 
     def decode_iter():
         torch.index_select(new_dev, 0, step_dev, out=new_buf)
         torch.index_select(q_dev, 0, step_dev, out=q_buf)
         for l in range(L):
-            attend_layer(l, new_buf, q_buf)
+            attend_layer(l)
         lens_dev.add_(1)
         step_dev.add_(1)
 
@@ -401,7 +406,7 @@ def run_ours(args, w, tt, rank, world, local_rank, dist, cpu_baseline_on):
     g_att, g_enc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_att, stream=cap, capture_error_mode="thread_local"):
         for l in range(L):
-            attend_layer(l, new_buf, q_buf)
+            attend_layer(l)
     with torch.cuda.graph(g_enc, stream=cap, capture_error_mode="thread_local"):
         for l in range(L):   # the prefill's own call: K and V of one layer in one launch
             encode_layer(l)
@@ -479,7 +484,7 @@ def run_ours(args, w, tt, rank, world, local_rank, dist, cpu_baseline_on):
             new_buf.copy_(inp.new[i:i + 1], non_blocking=True)
             q_buf.copy_(inp.q[i:i + 1], non_blocking=True)
             for l in range(L):
-                attend_layer(l, new_buf, q_buf)
+                attend_layer(l)
             lens_dev.add_(1)
             out_host[i].copy_(out_dev, non_blocking=True)
         ec.record(stream)

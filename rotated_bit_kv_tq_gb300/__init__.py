@@ -18,18 +18,20 @@ __all__ = ["TQ_TURBO2", "TQ_TURBO3", "TQ_BLOCK_VALUES", "NOALLOC_SCRATCH_BYTES",
            "inject_wait_timeout", "device_status", "load"]
 
 
+# Pointers and stream handles are passed as plain integers (the argtypes are c_void_p), which
+# keeps the per-call host cost of the decode loop low.
 def _stream_ptr(stream=None):
     import torch
     if stream is not None:
-        return ctypes.c_void_p(stream.cuda_stream)
+        return stream.cuda_stream
     raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
     if raw is not None:   # the current stream's handle without building a Stream object
-        return ctypes.c_void_p(raw(torch.cuda.current_device()))
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return raw(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    return t.data_ptr() if t is not None else None
 
 
 def block_bytes(tq_type: int) -> int:
@@ -87,6 +89,7 @@ class KVCache:
             for w in range(4):
                 self.view.rotation_signs[w] = (mask >> (32 * w)) & 0xFFFFFFFF
         self.view.norm_correction = 1 if norm_correction else 0
+        self.ref = ctypes.byref(self.view)   # what the C calls take (the view is updated in place)
 
     @property
     def nbytes(self) -> int:
@@ -98,7 +101,7 @@ def encode(cache: KVCache, src, *, seq_ids=None, positions=None, seq_id: int = 0
     """src: fp16 device tensor [n_tokens, n_kv_heads*head_dim] (row stride = src.stride(0))."""
     n = src.shape[0]
     stride = src.stride(0) if src.dim() > 1 else cache.n_kv_heads * cache.head_dim
-    check(load().tq_encode(ctypes.byref(cache.view), _ptr(src), n, stride, _ptr(seq_ids),
+    check(load().tq_encode(cache.ref, _ptr(src), n, stride, _ptr(seq_ids),
                            _ptr(positions), seq_id, pos0, _stream_ptr(stream)), "tq_encode")
 
 
@@ -110,13 +113,13 @@ def encode_kv(kc: KVCache, vc: KVCache, k_src, v_src, *, seq_ids=None, positions
         raise TQError(1, "encode_kv: K and V token counts differ")
     ks = k_src.stride(0) if k_src.dim() > 1 else kc.n_kv_heads * kc.head_dim
     vs = v_src.stride(0) if v_src.dim() > 1 else vc.n_kv_heads * vc.head_dim
-    check(load().tq_encode_kv(ctypes.byref(kc.view), ctypes.byref(vc.view), _ptr(k_src),
+    check(load().tq_encode_kv(kc.ref, vc.ref, _ptr(k_src),
                               _ptr(v_src), n, ks, vs, _ptr(seq_ids), _ptr(positions), seq_id,
                               pos0, _stream_ptr(stream)), "tq_encode_kv")
 
 
 def decode(cache: KVCache, seq_id: int, pos0: int, n_tokens: int, out, stream=None):
-    check(load().tq_decode(ctypes.byref(cache.view), seq_id, pos0, n_tokens, _ptr(out),
+    check(load().tq_decode(cache.ref, seq_id, pos0, n_tokens, _ptr(out),
                            _stream_ptr(stream)), "tq_decode")
 
 
@@ -129,7 +132,7 @@ def attn_decode(k: KVCache, v: KVCache, q, seq_lens, max_seq_len: int, out, work
     """q: fp16 [n_seqs, n_q_heads, head_dim]; seq_lens int32 [n_seqs]; out fp32 like q."""
     n_seqs, n_q_heads = q.shape[0], q.shape[1]
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    check(load().tq_attn_decode(ctypes.byref(k.view), ctypes.byref(v.view), _ptr(q), n_seqs,
+    check(load().tq_attn_decode(k.ref, v.ref, _ptr(q), n_seqs,
                                 n_q_heads, _ptr(seq_lens), max_seq_len, softmax_scale, _ptr(out),
                                 _ptr(workspace), ws_bytes, _stream_ptr(stream)), "tq_attn_decode")
 
@@ -140,7 +143,7 @@ def attn_decode_append(k: KVCache, v: KVCache, k_new, v_new, q, seq_lens, max_se
     seq_lens[s] - 1 of sequence s, then attention as attn_decode (seq_lens counts them)."""
     n_seqs, n_q_heads = q.shape[0], q.shape[1]
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    check(load().tq_attn_decode_append(ctypes.byref(k.view), ctypes.byref(v.view), _ptr(k_new),
+    check(load().tq_attn_decode_append(k.ref, v.ref, _ptr(k_new),
                                        _ptr(v_new), _ptr(q), n_seqs, n_q_heads, _ptr(seq_lens),
                                        max_seq_len, softmax_scale, _ptr(out), _ptr(workspace),
                                        ws_bytes, _stream_ptr(stream)), "tq_attn_decode_append")
@@ -152,7 +155,7 @@ def attn_prefill(k: KVCache, v: KVCache, q, out, *, pos0: int, seq_id: int = 0,
     position pos0 + j over cache rows 0 .. pos0 + j of seq_id (its own rows encoded
     first); out fp32 like q."""
     n_q, n_q_heads = q.shape[0], q.shape[1]
-    check(load().tq_attn_prefill(ctypes.byref(k.view), ctypes.byref(v.view), _ptr(q), seq_id,
+    check(load().tq_attn_prefill(k.ref, v.ref, _ptr(q), seq_id,
                                  pos0, n_q, n_q_heads, softmax_scale, _ptr(out),
                                  _stream_ptr(stream)), "tq_attn_prefill")
 
