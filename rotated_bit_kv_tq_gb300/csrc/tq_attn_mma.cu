@@ -30,6 +30,11 @@
 // Tiles of whole packed rows (all KV heads) are copied by TMA bulk copies (one per
 // contiguous run of rows, split at page boundaries) into a ring of shared-memory stages
 // completed through mbarriers; waits are bounded.
+//
+// Merge of the split partials (log-sum-exp): a single sequence whose splits fit one wave is
+// one cooperative launch whose CTAs merge the partials themselves (the grid merge below);
+// otherwise pairs of splits merge in distributed shared memory (one sequence) or every CTA
+// writes its own partial rows (batches), and the merge kernel of tq_attn.cu follows.
 #include <atomic>
 #include <cmath>
 
