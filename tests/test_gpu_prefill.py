@@ -101,6 +101,32 @@ def test_prefill_paged_cache_other_sequence(tq):
     _check(out.cpu().numpy().astype(np.float64), ref, "prefill paged seq 1")
 
 
+def test_prefill_head_dim_256_paged_cache_other_sequence(tq):
+    """head_dim 256 on sequence 1 of a paged cache (256-token pages in a seeded random order),
+    turbo2 K and turbo3 V, 2 KV heads (136- and 200-byte rows: the 2-byte staging path);
+    its 420 rows span two pages and seven 64-key tiles."""
+    w = synth.scaled(synth.BATCHED_PAGED, n_seqs=3, n_kv_heads=2, n_q_heads=8, head_dim=256)
+    pos0, n_q = 333, 87
+    n_rows = pos0 + n_q
+    pt, n_pages = synth.page_table(w, 512)
+    k = synth.kv_tokens(w, 0, "K", 0, n_rows, 1).reshape(n_rows, -1)
+    v = synth.kv_tokens(w, 0, "V", 0, n_rows, 1).reshape(n_rows, -1)
+    ptd = torch.from_numpy(pt).to(DEV)
+    kc = tq.KVCache(2, 2, 256, n_seqs=3, page_tokens=256, page_table=ptd, n_pages=n_pages)
+    vc = tq.KVCache(3, 2, 256, n_seqs=3, page_tokens=256, page_table=ptd, n_pages=n_pages)
+    tq.encode(kc, torch.from_numpy(k).to(DEV), seq_id=1)
+    tq.encode(vc, torch.from_numpy(v).to(DEV), seq_id=1)
+    q = _queries(w, 0, pos0, n_q, seq=1)
+    out = torch.full((n_q, 8, 256), float("nan"), device=DEV)
+    tq.attn_prefill(kc, vc, torch.from_numpy(q).to(DEV), out, pos0=pos0, seq_id=1)
+    assert tq.device_status() == 0
+    ref = oracle.attn_prefill(2, 3, oracle.encode_rows(2, k, 2, 256), oracle.encode_rows(3, v, 2, 256),
+                              q, pos0, 2, 256, 1 / np.sqrt(256))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    _check(got, ref, "prefill hd256 paged seq 1")
+
+
 def test_prefill_zero_queries_and_unsupported_shapes(tq):
     kc = tq.KVCache(3, 2, 128, capacity_tokens=8)
     out = torch.empty((0, 4, 128), device=DEV)

@@ -88,8 +88,8 @@ def test_attention_decode_with_variants(tq, hkv, hq):
     assert_attn_close(got, ref, "decode variants turbo3/2")
 
 
-def test_prefill_with_variants(tq):
-    hkv, hq, d, pos0, n_q = 8, 32, 128, 90, 40
+@pytest.mark.parametrize("hkv,hq,d,pos0,n_q", [(8, 32, 128, 90, 40), (4, 16, 256, 150, 40)])
+def test_prefill_with_variants(tq, hkv, hq, d, pos0, n_q):
     n = pos0 + n_q
     w = synth.scaled(synth.TINY, n_kv_heads=hkv, n_q_heads=hq, head_dim=d)
     k = synth.kv_tokens(w, 2, "K", 0, n).reshape(n, -1)
@@ -105,5 +105,5 @@ def test_prefill_with_variants(tq):
                               var_k=oracle.variant(signs=MASK_K, norm_correction=True),
                               var_v=oracle.variant(signs=MASK_V))
     got = out.cpu().numpy().astype(np.float64)
-    assert_attn_close(got, ref, "prefill variants turbo3/3")
-    assert_attn_close(got.reshape(n_q, -1), ref.reshape(n_q, -1), "prefill variants turbo3/3 (per token)")
+    assert_attn_close(got, ref, f"prefill variants turbo3/3 D{d}")
+    assert_attn_close(got.reshape(n_q, -1), ref.reshape(n_q, -1), f"prefill variants turbo3/3 D{d} (per token)")
