@@ -277,14 +277,15 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 // logical byte (block offset in the row) mod 4.
 constexpr int kTcWords = 16;   // logical words staged per key (covers 50 bytes at any offset)
 
+template <int KS = kTcKeys>   // keys per staging row (the word-major stride)
 __device__ __forceinline__ uint32_t wm_word(const uint32_t *raw, int j, int pt) {
-    return raw[j * kTcKeys + pt];
+    return raw[j * KS + pt];
 }
 
 // Producer thread pt of a group stages key pt of tile [t0, t0+128) of its cache: the
 // 4-byte words covering head g's block with cp.async when rows are 16-byte multiples (so
 // words are aligned), else the block's 2-byte halves with plain loads.
-template <int TYPE>
+template <int TYPE, int KS = kTcKeys>
 __device__ __forceinline__ void tc_stage(const CacheView &cv, int32_t seq, bool chunked,
                                          uint8_t *raw_bytes, uint8_t *ok, int g, int64_t t0,
                                          int64_t n_keys, int pt) {
@@ -297,14 +298,14 @@ __device__ __forceinline__ void tc_stage(const CacheView &cv, int32_t seq, bool 
         if (chunked) {
             for (int j = 0; j < nw; ++j)
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n"
-                             ::"r"(smem_u32(raw + j * kTcKeys + pt)), "l"(row + 4 * (w0 + j)) : "memory");
+                             ::"r"(smem_u32(raw + j * KS + pt)), "l"(row + 4 * (w0 + j)) : "memory");
         } else {
             // 2-byte aligned rows: halves h of the block go to logical byte (bo & 3) + 2h
             const uint16_t *src = reinterpret_cast<const uint16_t *>(row + bo);
             uint16_t *dst = reinterpret_cast<uint16_t *>(raw);
             for (int h = 0; h < bb / 2; ++h) {
                 const int lb = (bo & 3) + 2 * h;   // logical byte
-                dst[2 * ((lb >> 2) * kTcKeys + pt) + ((lb >> 1) & 1)] = src[h];
+                dst[2 * ((lb >> 2) * KS + pt) + ((lb >> 1) & 1)] = src[h];
             }
         }
     }
@@ -314,10 +315,12 @@ __device__ __forceinline__ void tc_stage(const CacheView &cv, int32_t seq, bool 
 // Producer thread pt decodes key pt of the staged tile of one cache: K into fp16 centroids
 // at tile[key][coord] (K-major) and its norm into norm[key]; V into fp16 |v| c (MN-major).
 // Absent rows get norm 0.
-template <int TYPE, bool MN>
+// KS: keys per staging row; NC, c_off (MN only): the tile holds NC coordinates and this block
+// fills coordinates c_off .. c_off + 127 (8-key groups NC * 16 bytes apart).
+template <int TYPE, bool MN, int KS = kTcKeys, int NC = 128>
 __device__ __forceinline__ void tc_decode(const uint8_t *raw_bytes, const uint8_t *ok, int g,
                                           const HalfTables &tab, uint8_t *tile, float *norm,
-                                          int pt) {
+                                          int pt, int c_off = 0) {
     constexpr int B = block_bytes(TYPE);
     const uint32_t *raw = reinterpret_cast<const uint32_t *>(raw_bytes);
     const int off = (g * B) & 3;               // the block's first logical byte
@@ -326,7 +329,7 @@ __device__ __forceinline__ void tc_decode(const uint8_t *raw_bytes, const uint8_
     // the norm: 2 bytes at logical byte off (off is even, so they share a word), 0 for an
     // absent row.  V folds it into the tile values (|v| c); K keeps it apart (norm[]) and
     // the scores are scaled in fp32, which keeps one fp16 rounding on the score path
-    const uint32_t w0 = wm_word(raw, 0, pt);
+    const uint32_t w0 = wm_word<KS>(raw, 0, pt);
     const __half nrm = ok[pt] ? __ushort_as_half((uint16_t)(w0 >> (8 * off))) : __ushort_as_half(0);
     const __half2 n2 = __halves2half2(nrm, nrm);
     if (!MN) norm[pt] = __half2float(nrm);
@@ -336,10 +339,10 @@ __device__ __forceinline__ void tc_decode(const uint8_t *raw_bytes, const uint8_
         // high-plane word at off + 34 + 4 q4 (word-aligned reads, then funnel shifts)
         const int jw = (off + 2 + 8 * q4) >> 2, jv = (off + 34 + 4 * q4) >> 2;
         Quarter<TYPE> qw;
-        const uint32_t a = wm_word(raw, jw, pt), b = wm_word(raw, jw + 1, pt), c = wm_word(raw, jw + 2, pt);
+        const uint32_t a = wm_word<KS>(raw, jw, pt), b = wm_word<KS>(raw, jw + 1, pt), c = wm_word<KS>(raw, jw + 2, pt);
         qw.W0 = __funnelshift_r(a, b, sh);
         qw.W1 = __funnelshift_r(b, c, sh);
-        if (TYPE == TQ_TURBO3) qw.V = __funnelshift_r(wm_word(raw, jv, pt), wm_word(raw, jv + 1, pt), sh);
+        if (TYPE == TQ_TURBO3) qw.V = __funnelshift_r(wm_word<KS>(raw, jv, pt), wm_word<KS>(raw, jv + 1, pt), sh);
         else qw.V = 0u;
 #pragma unroll
         for (int ww = 0; ww < 2; ++ww)
@@ -355,8 +358,9 @@ __device__ __forceinline__ void tc_decode(const uint8_t *raw_bytes, const uint8_
                     }
                 }
                 const int c0 = 32 * q4 + 16 * ww + 8 * r;
-                *reinterpret_cast<uint4 *>(tile + (MN ? canon_mn(pt, c0) : canon(pt, c0))) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
+                const uint32_t at = MN ? (uint32_t)(((c_off + c0) >> 3) * 128 + (pt >> 3) * (NC * 16) + (pt & 7) * 16)
+                                       : canon(pt, c0);
+                *reinterpret_cast<uint4 *>(tile + at) = make_uint4(o[0], o[1], o[2], o[3]);
             }
     }
 }
@@ -755,18 +759,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
 
 // ------------------------------------------------------------------ head_dim 256
 // Two 128-value blocks per head, each rotated and quantised on its own, each with its own
-// norm.  The scores need both blocks of the query and of every key; the query's high and
-// low fp16 parts over 256 coordinates (128 KB for 128 rows) then no longer fit in shared
-// memory beside the operand tiles, so they live in tensor memory as the A operand of the
-// score MMAs, and P moves to shared memory as the A operand of P V.  A key tile holds 64
-// keys, and the two blocks' products go to separate halves of the score buffer
-// (S_b = Q~_b C_b^T, N = 64 each), so each block is scaled by its own norm in fp32, as at
-// head_dim 128.  Each CTA produces one 128-coordinate block of the output (two CTAs per
-// query block, both computing the scores).
-// Tensor memory columns: S [0,128) (block 0 keys, then block 1 keys), O [128,256),
-// Q~ high [256,384), Q~ low [384,512).
+// norm.  One CTA per query block computes both output blocks:
+//  - tensor memory holds the scores S [0,128) (block 0's 64 keys, then block 1's: S_b =
+//    Q~_b C_b^T with N = 64, so each block is scaled by its own norm in fp32, as at head_dim
+//    128), the output O [128,384) (256 coordinates) and the query's high fp16 parts
+//    [384,512), the A operand of the high score MMAs;
+//  - shared memory holds the query's low parts (64 KB, the A operand of the low score MMAs),
+//    the K tile of 64 keys x 256 coordinates (double-buffered, one 16 KB tile per block), the
+//    V tile of 64 keys x 256 coordinates (single) and P (double), the A operand of P V, which
+//    is one N = 256 MMA per 16 keys.
+// The key norms are kept for three tiles: the K producer may decode tile i + 2 once tile i's
+// score MMAs are done, before the softmax has read tile i's norms.
 constexpr int k2Keys = 64;   // keys per tile
-constexpr uint32_t k2S = 0, k2O = 128, k2Qh = 256, k2Ql = 384;
+constexpr uint32_t k2S = 0, k2O = 128, k2Qh = 384;
 
 enum {
     k2BarQ = 0,        // queries written (256 arrivals)
@@ -774,38 +779,46 @@ enum {
     k2BarKFree = 3,    // [2] the tile's score MMAs done: K buffer free (commit)
     k2BarSFull = 5,    // scores ready (commit)
     k2BarSFree = 6,    // scores and norms read (256 arrivals)
-    k2BarVFull = 7,    // [2] V tile decoded (64 arrivals)
-    k2BarPFull = 9,    // [2] P written, O rescaled (256 arrivals)
-    k2BarPvFree = 11,  // [2] the tile's P V done: V tile and P buffer free (commit)
-    k2BarDrain = 13,   // every MMA of the CTA done (commit)
-    k2BarCount = 14
+    k2BarVFull = 7,    // V tile decoded (128 arrivals)
+    k2BarPFull = 8,    // [2] P written, O rescaled (256 arrivals)
+    k2BarPvFree = 10,  // [2] the tile's P V done: V tile and P buffer free (commit)
+    k2BarDrain = 12,   // every MMA of the CTA done (commit)
+    k2BarCount = 13
 };
 
 struct TcSmem256 {
+    alignas(1024) uint8_t ql[65536];       // Q~ low parts [row][coord 0..255], K-major
     alignas(1024) uint8_t k[2][2][16384];  // [buffer][block] K tile [key][coord], K-major
-    alignas(1024) uint8_t v[2][16384];     // [buffer] V tile of the output block, MN-major
+    alignas(1024) uint8_t v[32768];        // V tile [key][coord 0..255], MN-major
     alignas(1024) uint8_t p[2][16384];     // [buffer] P [row][key] fp16, K-major
-    alignas(1024) uint8_t xo[65536];       // epilogue: the two halves of every output row
-    alignas(16) uint8_t raw_k[2][kTcKeys * 64];   // staged K blocks (word-major, stride kTcKeys)
-    alignas(16) uint8_t raw_v[kTcKeys * 64];
+    alignas(16) uint8_t raw_k[2][k2Keys * 64];   // staged K blocks (word-major, 64 keys a row)
+    alignas(16) uint8_t raw_v[2][k2Keys * 64];   // staged V blocks
     // [tile mod 3][block][key] norms: the producer writes tile i + 2's norms once tile i's
     // score MMAs are done, possibly before the softmax has read tile i's
     float kn[3][2][k2Keys];
     float xch[2][2][kTcRows];
-    uint8_t ok[3][kTcKeys];                // K block 0, K block 1, V: key present
+    uint8_t ok[4][k2Keys];                 // K block 0, K block 1, V block 0, V block 1
     alignas(8) uint64_t bar[k2BarCount];
     uint32_t tmem;
 };
 
+// Element (row, coord) of the 256-coordinate K-major query tile: 32 core matrices along K,
+// so 8-row groups sit 4096 bytes apart.
+__device__ __forceinline__ uint32_t canon256(int r, int c) {
+    return (uint32_t)((r >> 3) * 4096 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
 // Element (row, key) of a 64-key K-major tile: 8 core matrices along K, so 8-row groups sit
 // 1024 bytes apart.
 __device__ __forceinline__ uint32_t canon64(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
 }
-// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B (both K-major), M = 128,
-// N = 64.
+// Instruction descriptors, kind::f16 (fp32 accumulate, fp16 A and B, M = 128): the score MMA
+// (both operands K-major, N = 64) and P V (B MN-major, N = 256).
 constexpr uint32_t idesc_f16_n64() {
     return (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+}
+constexpr uint32_t idesc_f16_pv256() {
+    return (1u << 4) | (1u << 16) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 template <int TK, int TV>
@@ -816,9 +829,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
     TcSmem256 &sm = *reinterpret_cast<TcSmem256 *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     __shared__ int abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // CTA 2 q + ob produces output block ob of query CTA q (longest first, as above)
-    const int ob = (int)(blockIdx.x & 1u);
-    const unsigned qcta = blockIdx.x >> 1;
+    const unsigned qcta = blockIdx.x;   // longest first, as above
     const int g = (int)(qcta % (unsigned)p.n_kv_heads), G = p.group, Hq = p.n_q_heads;
     const int64_t j0 = (p.n_qblocks - 1 - (int64_t)(qcta / (unsigned)p.n_kv_heads)) * p.bq;
     const int64_t j_end = min64(p.n_q, j0 + p.bq);
@@ -833,10 +844,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
         tc_bar_init(bar(k2BarQ), kTcSoftmax);
         tc_bar_init(bar(k2BarSFull), 1);
         tc_bar_init(bar(k2BarSFree), kTcSoftmax);
+        tc_bar_init(bar(k2BarVFull), kTcGroup);
         for (int b = 0; b < 2; ++b) {
             tc_bar_init(bar(k2BarKFull + b), kTcGroup);
             tc_bar_init(bar(k2BarKFree + b), 1);
-            tc_bar_init(bar(k2BarVFull + b), k2Keys);
             tc_bar_init(bar(k2BarPFull + b), kTcSoftmax);
             tc_bar_init(bar(k2BarPvFree + b), 1);
         }
@@ -862,8 +873,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
         const int64_t qpos = valid ? p.pos0 + j0 + jl : INT64_MAX;
         const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
         const uint32_t pair_bar = 3u + (uint32_t)quad;
-        // the query, block by block: coords 64 h .. 64 h + 63 of Q~_b = H (D q_b) * scale,
-        // hi and lo fp16 parts into tensor memory (two K values per column)
+        // the query, block by block: coords 64 h .. 64 h + 63 of Q~_b = H (D q_b) * scale;
+        // high fp16 parts into tensor memory (two K values per column), low parts into the
+        // shared-memory tile
 #pragma unroll 1
         for (int blk = 0; blk < 2; ++blk) {
             float x[64];
@@ -904,10 +916,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
                     split_half2(x[32 * c + 2 * e] * p.score_scale, x[32 * c + 2 * e + 1] * p.score_scale,
                                 w[e], wl[e]);
                 tc_st16(tmem + lane_base + k2Qh + 64u * blk + 32u * h + 16u * c, w);
-                tc_st16(tmem + lane_base + k2Ql + 64u * blk + 32u * h + 16u * c, wl);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4 *>(sm.ql + canon256(r, kBlock * blk + 64 * h + 32 * c + 8 * q4)) =
+                        make_uint4(wl[4 * q4], wl[4 * q4 + 1], wl[4 * q4 + 2], wl[4 * q4 + 3]);
             }
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         tc_arrive(bar(k2BarQ));
 
@@ -973,16 +989,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
             const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
             l_run = l_run * alpha + psum;
             if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // the running output must hold every P V up to tile i - 1 before it is scaled;
+                // this half scales output columns 128 h .. 128 h + 127
                 if (!*abort_v && !tc_wait(bar(k2BarPvFree + ((i - 1) & 1)), (uint32_t)(((i - 1) >> 1) & 1)))
                     *abort_v = 1;
                 tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
                     float t[32];
-                    tc_ld32(tmem + lane_base + k2O + 64u * h + 32u * c, t);
+                    tc_ld32(tmem + lane_base + k2O + 128u * h + 32u * c, t);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) t[e] *= alpha;
-                    tc_st32(tmem + lane_base + k2O + 64u * h + 32u * c, t);
+                    tc_st32(tmem + lane_base + k2O + 128u * h + 32u * c, t);
                 }
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -990,94 +1008,105 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
             tc_fence_before();
             tc_arrive(bar(k2BarPFull + b));
         }
-        // ---- epilogue: O / l for output block ob, inverse rotation, V signs, store
+        // ---- epilogue: O / l, block by block: inverse rotation, V signs, store
         const bool done = n_tiles > 0 && !*abort_v &&
                           tc_wait(bar(k2BarPvFree + ((n_tiles - 1) & 1)), (uint32_t)(((n_tiles - 1) >> 1) & 1));
         tc_fence_after();
         sm.xch[n_tiles & 1][h][r] = l_run;
-        float o[64];
-        if (n_tiles > 0) {
-            tc_ld64(tmem + lane_base + k2O + 64u * h, o);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 64; ++e) o[e] = 0.f;
-        }
-        fwht64(o);
-        float *xo = reinterpret_cast<float *>(sm.xo);
-        auto xo_at = [&](int row, int c4) { return xo + row * 128 + (((c4 ^ row) & 31) << 2); };
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-            *reinterpret_cast<float4 *>(xo_at(r, 16 * h + c)) =
-                make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         named_sync(pair_bar, 64);
         const float l_row = l_run + sm.xch[n_tiles & 1][h ^ 1][r];
+        const float inv = l_row > 0.f ? p.out_scale / l_row : 0.f;
+        // the query's low-part tile is idle once every MMA has completed
+        float *xo = reinterpret_cast<float *>(sm.ql);
+        auto xo_at = [&](int row, int c4) { return xo + row * 128 + (((c4 ^ row) & 31) << 2); };
+#pragma unroll 1
+        for (int blk = 0; blk < 2; ++blk) {
+            float o[64];
+            if (n_tiles > 0) {
+                tc_ld64(tmem + lane_base + k2O + 128u * blk + 64u * h, o);
+            } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const float4 u = *reinterpret_cast<const float4 *>(xo_at(r, 16 * (h ^ 1) + c));
-            const float pv[4] = {u.x, u.y, u.z, u.w};
+                for (int e = 0; e < 64; ++e) o[e] = 0.f;
+            }
+            fwht64(o);
+            if (blk > 0) named_sync(pair_bar, 64);   // the partner has read the last block's halves
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[4 * c + e] = h ? pv[e] - o[4 * c + e] : o[4 * c + e] + pv[e];
-        }
-        if (valid && done) {
-            const float inv = l_row > 0.f ? p.out_scale / l_row : 0.f;
-            float4 *dst = reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)D +
-                                                     kBlock * ob + 64 * h);
+            for (int c = 0; c < 16; ++c)
+                *reinterpret_cast<float4 *>(xo_at(r, 16 * h + c)) =
+                    make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            named_sync(pair_bar, 64);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                float v4[4];
+                const float4 u = *reinterpret_cast<const float4 *>(xo_at(r, 16 * (h ^ 1) + c));
+                const float pv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    v4[e] = __uint_as_float(__float_as_uint(o[4 * c + e] * inv) ^ sign_mask(p.vc, 64 * h + 4 * c + e));
-                dst[c] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+                for (int e = 0; e < 4; ++e) o[4 * c + e] = h ? pv[e] - o[4 * c + e] : o[4 * c + e] + pv[e];
+            }
+            if (valid && done) {
+                float4 *dst = reinterpret_cast<float4 *>(p.out + ((j0 + jl) * Hq + g * G + hl) * (int64_t)D +
+                                                         kBlock * blk + 64 * h);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    float v4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        v4[e] = __uint_as_float(__float_as_uint(o[4 * c + e] * inv) ^ sign_mask(p.vc, 64 * h + 4 * c + e));
+                    dst[c] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+                }
             }
         }
     } else if (warp < kTcMmaWarp) {
+        // ================= producers: thread (block, key) of the K group (warps 8-11) and of
+        // the V group (warps 12-15)
         const int pt = (tid - kTcSoftmax) & (kTcGroup - 1);
-        const int key = pt & (k2Keys - 1);
+        const int key = pt & (k2Keys - 1), blk = pt >> 6;
         if (tid - kTcSoftmax < kTcGroup) {
-            // ================= K producers: thread (block, key), double-buffered
-            const int blk = pt >> 6;
+            // K: double-buffered tiles, one 16 KB tile per block
             const HalfTables tab = make_tables<TK>();
-            if (n_tiles > 0) tc_stage<TK>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk, 0, n_keys, key);
+            if (n_tiles > 0)
+                tc_stage<TK, k2Keys>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk, 0, n_keys, key);
             cp_async_commit();
             for (int i = 0; i < n_tiles; ++i) {
                 const int b = i & 1;
                 cp_async_wait<0>();
                 if (i >= 2 && !*abort_v && !tc_wait(bar(k2BarKFree + b), (uint32_t)(((i - 2) >> 1) & 1)))
                     *abort_v = 1;
-                tc_decode<TK, false>(sm.raw_k[blk], sm.ok[blk], 2 * g + blk, tab, sm.k[b][blk], sm.kn[i % 3][blk], key);
+                tc_decode<TK, false, k2Keys>(sm.raw_k[blk], sm.ok[blk], 2 * g + blk, tab, sm.k[b][blk],
+                                             sm.kn[i % 3][blk], key);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_arrive(bar(k2BarKFull + b));
                 if (i + 1 < n_tiles)
-                    tc_stage<TK>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk,
-                                 (int64_t)(i + 1) * k2Keys, n_keys, key);
+                    tc_stage<TK, k2Keys>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk,
+                                         (int64_t)(i + 1) * k2Keys, n_keys, key);
                 cp_async_commit();
             }
             cp_async_wait<0>();
-        } else if (pt < k2Keys) {
-            // ================= V producers: the output block of every key, double-buffered
+        } else {
+            // V: one 256-coordinate tile, rewritten once the previous tile's P V is done
             const HalfTables tab = make_tables<TV>();
-            if (n_tiles > 0) tc_stage<TV>(p.vc, p.seq, p.chunked_v, sm.raw_v, sm.ok[2], 2 * g + ob, 0, n_keys, key);
+            if (n_tiles > 0)
+                tc_stage<TV, k2Keys>(p.vc, p.seq, p.chunked_v, sm.raw_v[blk], sm.ok[2 + blk], 2 * g + blk, 0, n_keys, key);
             cp_async_commit();
             for (int i = 0; i < n_tiles; ++i) {
-                const int b = i & 1;
                 cp_async_wait<0>();
-                if (i >= 2 && !*abort_v &&
-                    !tc_wait(bar(k2BarPvFree + b), (uint32_t)(((i - 2) >> 1) & 1)))
+                if (i >= 1 && !*abort_v &&
+                    !tc_wait(bar(k2BarPvFree + ((i - 1) & 1)), (uint32_t)(((i - 1) >> 1) & 1)))
                     *abort_v = 1;
-                tc_decode<TV, true>(sm.raw_v, sm.ok[2], 2 * g + ob, tab, sm.v[b], nullptr, key);
+                tc_decode<TV, true, k2Keys, D>(sm.raw_v[blk], sm.ok[2 + blk], 2 * g + blk, tab, sm.v, nullptr,
+                                               key, kBlock * blk);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                tc_arrive(bar(k2BarVFull + b));
+                tc_arrive(bar(k2BarVFull));
                 if (i + 1 < n_tiles)
-                    tc_stage<TV>(p.vc, p.seq, p.chunked_v, sm.raw_v, sm.ok[2], 2 * g + ob,
-                                 (int64_t)(i + 1) * k2Keys, n_keys, key);
+                    tc_stage<TV, k2Keys>(p.vc, p.seq, p.chunked_v, sm.raw_v[blk], sm.ok[2 + blk], 2 * g + blk,
+                                         (int64_t)(i + 1) * k2Keys, n_keys, key);
                 cp_async_commit();
             }
             cp_async_wait<0>();
         }
     } else if (lane == 0) {
         // ================= MMA issue (one thread)
-        constexpr uint32_t idesc_s = idesc_f16_n64(), idesc_pv = idesc_f16(true);
+        constexpr uint32_t idesc_s = idesc_f16_n64(), idesc_pv = idesc_f16_pv256();
+        const uint32_t ql_base = smem_u32(sm.ql), v_base = smem_u32(sm.v);
         bool ok = tc_wait(bar(k2BarQ), 0);
         int ns = 0, npv = 0;
         uint32_t idle = 0;
@@ -1087,8 +1116,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
             if (ns < n_tiles && tc_test(bar(k2BarKFull + (ns & 1)), (uint32_t)((ns >> 1) & 1)) &&
                 (ns == 0 || tc_test(bar(k2BarSFree), (uint32_t)((ns - 1) & 1)))) {
                 tc_fence_after();
-                // S_b = Q~_b C_b^T: A = Q~ block b from tensor memory (16 coords = 8 columns per
-                // MMA), B = the block's K tile; high parts, then low parts
+                // S_b = Q~_b C_b^T: the high parts from tensor memory (16 coords = 8 columns per
+                // MMA), the low parts from shared memory; B = the block's K tile
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
                     const uint32_t k_base = smem_u32(sm.k[ns & 1][blk]);
@@ -1098,8 +1127,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
                                   sdesc(k_base + 256u * kk, 128, 2048), idesc_s, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        tc_mma_ts(tmem + k2S + 64u * blk, tmem + k2Ql + 64u * blk + 8u * kk,
-                                  sdesc(k_base + 256u * kk, 128, 2048), idesc_s, 1u);
+                        tc_mma(tmem + k2S + 64u * blk, sdesc(ql_base + 2048u * blk + 256u * kk, 128, 4096),
+                               sdesc(k_base + 256u * kk, 128, 2048), idesc_s, 1u);
                 }
                 tc_commit(bar(k2BarSFull));
                 tc_commit(bar(k2BarKFree + (ns & 1)));
@@ -1107,15 +1136,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
                 progressed = true;
             }
             if (npv < ns && tc_test(bar(k2BarPFull + (npv & 1)), (uint32_t)((npv >> 1) & 1)) &&
-                tc_test(bar(k2BarVFull + (npv & 1)), (uint32_t)((npv >> 1) & 1))) {
+                tc_test(bar(k2BarVFull), (uint32_t)(npv & 1))) {
                 tc_fence_after();
                 const int b = npv & 1;
-                const uint32_t p_base = smem_u32(sm.p[b]), v_base = smem_u32(sm.v[b]);
-                // A = P from shared memory (16 keys per MMA), B = the V tile
+                const uint32_t p_base = smem_u32(sm.p[b]);
+                // A = P from shared memory (16 keys per MMA), B = the V tile, N = 256
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma(tmem + k2O, sdesc(p_base + 256u * kk, 128, 1024),
-                           sdesc(v_base + 4096u * kk, 2048, 128), idesc_pv, (npv > 0 || kk > 0));
+                           sdesc(v_base + 8192u * kk, 4096, 128), idesc_pv, (npv > 0 || kk > 0));
                 tc_commit(bar(k2BarPvFree + b));
                 ++npv;
                 progressed = true;
@@ -1144,7 +1173,7 @@ tq_status launch_tc256_t(const TcParams &p, unsigned n_ctas, cudaStream_t stream
     const tq_status st = kernel_setup(reinterpret_cast<const void *>(prefill_tc256_kernel<TK, TV>),
                                       (int)smem, kTcThreads, nullptr);
     if (st != TQ_OK) return st;
-    PdlConfig lc(dim3(2 * n_ctas), dim3(kTcThreads), smem, stream);
+    PdlConfig lc(dim3(n_ctas), dim3(kTcThreads), smem, stream);
     return check_cuda(cudaLaunchKernelEx(&lc.cfg, prefill_tc256_kernel<TK, TV>, p));
 }
 
@@ -1199,7 +1228,7 @@ tq_status launch_prefill(const tq_cache &k, const tq_cache &v, const void *q, in
     const int64_t n_ctas = p.n_qblocks * k.n_kv_heads;
     if (n_ctas > 0x3fffffff) return TQ_ERR_UNSUPPORTED;
     const unsigned nc = (unsigned)n_ctas;
-    if (k.head_dim == 2 * kBlock) {   // two CTAs (output blocks) per query block, no key split
+    if (k.head_dim == 2 * kBlock) {   // one CTA per query block, no key split
         p.split = 1;
         if (k.type == TQ_TURBO3 && v.type == TQ_TURBO3) return launch_tc256_t<3, 3>(p, nc, stream);
         if (k.type == TQ_TURBO2 && v.type == TQ_TURBO2) return launch_tc256_t<2, 2>(p, nc, stream);
