@@ -770,7 +770,8 @@ TRACE_PHASES = {
                   "loop end (slowest warp)",
                   "epilogue done (cluster barrier; grid merge: partial rows stored)",
                   "cluster merge done (grid merge: grid barrier passed)",
-                  "grid merge: rows loaded", "grid merge: output stored"],
+                  "grid merge: rows loaded", "grid merge: output stored",
+                  "warps of each KV head combined"],
     "merge": ["entry", "dependency wait returned", "partial rows loaded", "output stored"],
 }
 
