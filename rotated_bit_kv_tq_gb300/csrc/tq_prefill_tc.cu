@@ -93,7 +93,7 @@ struct TcSmem {
     alignas(1024) uint8_t ql[32768];       // Q~ low parts (fp16 rounding of the remainder)
     alignas(1024) uint8_t k[2][32768];     // K tile [key][coord], K-major
     alignas(1024) uint8_t v[2][32768];     // V tile [key][coord], coords contiguous (MN-major)
-    alignas(16) uint8_t raw[2][kTcKeys * 64];   // staged blocks of one tile (K, V), word-major
+    alignas(16) uint8_t raw[2][kTcKeys * 64];   // staged blocks of one tile (K, V), 64-byte key windows
     float kn[2][kTcKeys];                  // K norms of the two tile buffers
     float xch[2][2][kTcRows];              // [tile parity][half][row] row maxima, then sums
     uint8_t ok[2][kTcKeys];                // [K/V][key] row present
@@ -270,79 +270,98 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Staged tile bytes are word-major: logical word j (4 bytes) of key k sits at word
-// j * 128 + k of the cache's staging area, so that the decode threads (one per key) read
-// the same logical word of 32 consecutive keys from 32 different banks.  Logical byte 0 is
-// the first byte of the 4-byte word holding the block's first byte; the block starts at
-// logical byte (block offset in the row) mod 4.
-constexpr int kTcWords = 16;   // logical words staged per key (covers 50 bytes at any offset)
-
-template <int KS = kTcKeys>   // keys per staging row (the word-major stride)
-__device__ __forceinline__ uint32_t wm_word(const uint32_t *raw, int j, int pt) {
-    return raw[j * KS + pt];
+// Staged tile bytes are key-major: key k owns the 64 bytes at k * 64 of the cache's staging
+// area, a window of its row that starts at the 16-byte boundary at or below the block (the
+// block sits at window byte (block offset in the row) mod 16, and 14 + 50 bytes fit).  The
+// window's 16-byte chunk c is stored at chunk c ^ ((k >> 1) & 3), so that 8 consecutive keys'
+// 16-byte accesses to one chunk cover the 32 banks once (the copies that fill it, and the
+// decode threads, one per key, reading it back).
+__device__ __forceinline__ uint32_t win_chunk(int key, int c) {
+    return (uint32_t)(key * 64 + ((c ^ ((key >> 1) & 3)) << 4));
 }
 
-// Producer thread pt of a group stages key pt of tile [t0, t0+128) of its cache: the
-// 4-byte words covering head g's block with cp.async when rows are 16-byte multiples (so
-// words are aligned), else the block's 2-byte halves with plain loads.
-template <int TYPE, int KS = kTcKeys>
+// Producer thread pt of a group stages key pt of tile [t0, t0 + keys) of its cache: the
+// 16-byte chunks covering head g's block with cp.async when rows are 16-byte multiples (so
+// the chunks are aligned and lie inside the row), else the block's 2-byte halves with plain
+// loads.
+template <int TYPE>
 __device__ __forceinline__ void tc_stage(const CacheView &cv, int32_t seq, bool chunked,
-                                         uint8_t *raw_bytes, uint8_t *ok, int g, int64_t t0,
+                                         uint8_t *raw, uint8_t *ok, int g, int64_t t0,
                                          int64_t n_keys, int pt) {
     const int64_t t = t0 + pt;
     const uint8_t *row = t < n_keys ? row_ptr(cv, seq, t) : nullptr;
     constexpr int bb = block_bytes(TYPE);
-    const int bo = g * bb, w0 = bo >> 2, nw = ((bo + bb + 3) >> 2) - w0;
-    uint32_t *raw = reinterpret_cast<uint32_t *>(raw_bytes);
+    const int bo = g * bb, x0 = bo & ~15, lead = bo & 15;
     if (row) {
         if (chunked) {
-            for (int j = 0; j < nw; ++j)
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n"
-                             ::"r"(smem_u32(raw + j * KS + pt)), "l"(row + 4 * (w0 + j)) : "memory");
+            const int nc = (lead + bb + 15) >> 4;   // chunks up to the one holding the last byte
+            for (int c = 0; c < nc; ++c) cp_async16(smem_u32(raw + win_chunk(pt, c)), row + x0 + 16 * c);
         } else {
-            // 2-byte aligned rows: halves h of the block go to logical byte (bo & 3) + 2h
+            // 2-byte aligned rows: half h of the block goes to window byte lead + 2h
             const uint16_t *src = reinterpret_cast<const uint16_t *>(row + bo);
-            uint16_t *dst = reinterpret_cast<uint16_t *>(raw);
             for (int h = 0; h < bb / 2; ++h) {
-                const int lb = (bo & 3) + 2 * h;   // logical byte
-                dst[2 * ((lb >> 2) * KS + pt) + ((lb >> 1) & 1)] = src[h];
+                const int wb = lead + 2 * h;
+                *reinterpret_cast<uint16_t *>(raw + win_chunk(pt, wb >> 4) + (wb & 15)) = src[h];
             }
         }
     }
     ok[pt] = row ? 1 : 0;
 }
 
-// Producer thread pt decodes key pt of the staged tile of one cache: K into fp16 centroids
-// at tile[key][coord] (K-major) and its norm into norm[key]; V into fp16 |v| c (MN-major).
-// Absent rows get norm 0.
-// KS: keys per staging row; NC, c_off (MN only): the tile holds NC coordinates and this block
-// fills coordinates c_off .. c_off + 127 (8-key groups NC * 16 bytes apart).
-template <int TYPE, bool MN, int KS = kTcKeys, int NC = 128>
-__device__ __forceinline__ void tc_decode(const uint8_t *raw_bytes, const uint8_t *ok, int g,
+// Producer thread pt reads key pt's staged window and brings its block to byte 0:
+// n[j] = block bytes 4j .. 4j + 3.  The block's offset in the window, lead (its offset in the
+// row mod 16), is the same for all keys of a warp; one code path serves every head (a form
+// templated on lead overflowed the instruction cache): a word shift by lead >> 2 in two
+// select levels, then a funnel shift by the remaining 0 or 2 bytes.  The staging area is
+// free again once this returns.
+template <int TYPE>
+__device__ __forceinline__ void tc_window(const uint8_t *raw, int g, int pt, uint32_t (&n)[13]) {
+    constexpr int B = block_bytes(TYPE);
+    uint32_t w[17];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(raw + win_chunk(pt, c));
+        w[4 * c] = u.x;
+        w[4 * c + 1] = u.y;
+        w[4 * c + 2] = u.z;
+        w[4 * c + 3] = u.w;
+    }
+    w[16] = 0u;
+    const int lead = (g * B) & 15;
+    const bool s1 = lead & 4, s2 = lead & 8;
+    const uint32_t sh = 8u * (uint32_t)(lead & 3);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = s1 ? w[j + 1] : w[j];
+#pragma unroll
+    for (int j = 0; j < 14; ++j) w[j] = s2 ? w[j + 2] : w[j];
+#pragma unroll
+    for (int j = 0; j < 13; ++j) n[j] = __funnelshift_r(w[j], w[j + 1], sh);
+}
+
+// Producer thread pt decodes key pt from its block bytes n (tc_window): K into fp16
+// centroids at tile[key][coord] (K-major) and its norm into norm[key]; V into fp16 |v| c
+// (MN-major).  Absent rows get norm 0.
+// NC, c_off (MN only): the tile holds NC coordinates and this block fills coordinates
+// c_off .. c_off + 127 (8-key groups NC * 16 bytes apart).
+template <int TYPE, bool MN, int NC = 128>
+__device__ __forceinline__ void tc_decode(const uint32_t (&n)[13], bool present,
                                           const HalfTables &tab, uint8_t *tile, float *norm,
                                           int pt, int c_off = 0) {
-    constexpr int B = block_bytes(TYPE);
-    const uint32_t *raw = reinterpret_cast<const uint32_t *>(raw_bytes);
-    const int off = (g * B) & 3;               // the block's first logical byte
-    const uint32_t sh = (uint32_t)((off + 2) & 3) * 8u;
     const Shifts shifts = {2u, 4u, 1u << 16, 1u << 30, 1u << 31};
-    // the norm: 2 bytes at logical byte off (off is even, so they share a word), 0 for an
-    // absent row.  V folds it into the tile values (|v| c); K keeps it apart (norm[]) and
-    // the scores are scaled in fp32, which keeps one fp16 rounding on the score path
-    const uint32_t w0 = wm_word<KS>(raw, 0, pt);
-    const __half nrm = ok[pt] ? __ushort_as_half((uint16_t)(w0 >> (8 * off))) : __ushort_as_half(0);
+    // the norm: block bytes 0-1, 0 for an absent row.  V folds it into the tile values
+    // (|v| c); K keeps it apart (norm[]) and the scores are scaled in fp32, which keeps one
+    // fp16 rounding on the score path
+    const __half nrm = present ? __ushort_as_half((uint16_t)(n[0] & 0xffffu)) : __ushort_as_half(0);
     const __half2 n2 = __halves2half2(nrm, nrm);
     if (!MN) norm[pt] = __half2float(nrm);
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
-        // the quarter's low-plane bytes start at logical byte off + 2 + 8 q4, its
-        // high-plane word at off + 34 + 4 q4 (word-aligned reads, then funnel shifts)
-        const int jw = (off + 2 + 8 * q4) >> 2, jv = (off + 34 + 4 * q4) >> 2;
+        // the quarter's low-plane bytes are block bytes 2 + 8 q4 .., its high-plane word
+        // block bytes 34 + 4 q4 ..
         Quarter<TYPE> qw;
-        const uint32_t a = wm_word<KS>(raw, jw, pt), b = wm_word<KS>(raw, jw + 1, pt), c = wm_word<KS>(raw, jw + 2, pt);
-        qw.W0 = __funnelshift_r(a, b, sh);
-        qw.W1 = __funnelshift_r(b, c, sh);
-        if (TYPE == TQ_TURBO3) qw.V = __funnelshift_r(wm_word<KS>(raw, jv, pt), wm_word<KS>(raw, jv + 1, pt), sh);
+        qw.W0 = __funnelshift_r(n[2 * q4], n[2 * q4 + 1], 16);
+        qw.W1 = __funnelshift_r(n[2 * q4 + 1], n[2 * q4 + 2], 16);
+        if (TYPE == TQ_TURBO3) qw.V = __funnelshift_r(n[8 + q4], n[9 + q4], 16);
         else qw.V = 0u;
 #pragma unroll
         for (int ww = 0; ww < 2; ++ww)
@@ -379,10 +398,11 @@ __device__ __forceinline__ void fwht64(float (&x)[64]) {
 }
 
 // One producer group: stage and decode every tile of its cache (K: centroids and norms;
-// V: |v| c), double-buffered.  Each thread reads back only the words it staged itself, so
-// the group needs no barrier of its own; tile buffer b is rewritten once the consumers of
-// tile i - 2 are done with it (K: the softmax has read that tile's scores and norms; V: its
-// P V has completed).
+// V: |v| c), double-buffered.  Each thread reads back only the bytes it staged itself, so
+// the group needs no barrier of its own.  Tile i's bytes are read into registers first, and
+// tile i + 1's copies go out before the wait for the tile buffer: tile buffer b is rewritten
+// once the consumers of tile i - 2 are done with it (K: the softmax has read that tile's
+// scores and norms; V: its P V has completed).
 template <int TYPE, bool IS_V>
 __device__ __forceinline__ void tc_produce(const TcParams &p, TcSmem &sm, int g, int64_t n_keys,
                                            int tile0, int n_tiles, int pt, volatile int *abort_v) {
@@ -396,16 +416,19 @@ __device__ __forceinline__ void tc_produce(const TcParams &p, TcSmem &sm, int g,
     cp_async_commit();
     for (int i = 0; i < n_tiles; ++i) {
         const int b = i & 1;
-        cp_async_wait<0>();   // this thread's words of tile i have landed
+        cp_async_wait<0>();   // this thread's bytes of tile i have landed
+        uint32_t nb[13];
+        tc_window<TYPE>(raw, g, pt, nb);
+        const bool present = ok[pt] != 0;
+        if (i + 1 < n_tiles) tc_stage<TYPE>(cv, p.seq, chunked, raw, ok, g, (int64_t)(tile0 + i + 1) * kTcKeys, n_keys, pt);
+        cp_async_commit();
         if (i >= 2 && !*abort_v &&
             !tc_wait(smem_u32(&sm.bar[free_bar + b]), (uint32_t)(((i - 2) >> 1) & 1)))
             *abort_v = 1;
-        if (IS_V) tc_decode<TYPE, true>(raw, ok, g, tab, sm.v[b], nullptr, pt);
-        else tc_decode<TYPE, false>(raw, ok, g, tab, sm.k[b], sm.kn[b], pt);
+        if (IS_V) tc_decode<TYPE, true>(nb, present, tab, sm.v[b], nullptr, pt);
+        else tc_decode<TYPE, false>(nb, present, tab, sm.k[b], sm.kn[b], pt);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_arrive(smem_u32(&sm.bar[full_bar + b]));
-        if (i + 1 < n_tiles) tc_stage<TYPE>(cv, p.seq, chunked, raw, ok, g, (int64_t)(tile0 + i + 1) * kTcKeys, n_keys, pt);
-        cp_async_commit();
     }
     cp_async_wait<0>();
 }
@@ -791,7 +814,7 @@ struct TcSmem256 {
     alignas(1024) uint8_t k[2][2][16384];  // [buffer][block] K tile [key][coord], K-major
     alignas(1024) uint8_t v[32768];        // V tile [key][coord 0..255], MN-major
     alignas(1024) uint8_t p[2][16384];     // [buffer] P [row][key] fp16, K-major
-    alignas(16) uint8_t raw_k[2][k2Keys * 64];   // staged K blocks (word-major, 64 keys a row)
+    alignas(16) uint8_t raw_k[2][k2Keys * 64];   // staged K blocks (64-byte key windows)
     alignas(16) uint8_t raw_v[2][k2Keys * 64];   // staged V blocks
     // [tile mod 3][block][key] norms: the producer writes tile i + 2's norms once tile i's
     // score MMAs are done, possibly before the softmax has read tile i's
@@ -1064,42 +1087,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc256_kernel(const TcPa
             // K: double-buffered tiles, one 16 KB tile per block
             const HalfTables tab = make_tables<TK>();
             if (n_tiles > 0)
-                tc_stage<TK, k2Keys>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk, 0, n_keys, key);
+                tc_stage<TK>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk, 0, n_keys, key);
             cp_async_commit();
             for (int i = 0; i < n_tiles; ++i) {
                 const int b = i & 1;
                 cp_async_wait<0>();
+                uint32_t nb[13];
+                tc_window<TK>(sm.raw_k[blk], 2 * g + blk, key, nb);
+                const bool present = sm.ok[blk][key] != 0;
+                if (i + 1 < n_tiles)
+                    tc_stage<TK>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk,
+                                 (int64_t)(i + 1) * k2Keys, n_keys, key);
+                cp_async_commit();
                 if (i >= 2 && !*abort_v && !tc_wait(bar(k2BarKFree + b), (uint32_t)(((i - 2) >> 1) & 1)))
                     *abort_v = 1;
-                tc_decode<TK, false, k2Keys>(sm.raw_k[blk], sm.ok[blk], 2 * g + blk, tab, sm.k[b][blk],
-                                             sm.kn[i % 3][blk], key);
+                tc_decode<TK, false>(nb, present, tab, sm.k[b][blk], sm.kn[i % 3][blk], key);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_arrive(bar(k2BarKFull + b));
-                if (i + 1 < n_tiles)
-                    tc_stage<TK, k2Keys>(p.kc, p.seq, p.chunked_k, sm.raw_k[blk], sm.ok[blk], 2 * g + blk,
-                                         (int64_t)(i + 1) * k2Keys, n_keys, key);
-                cp_async_commit();
             }
             cp_async_wait<0>();
         } else {
             // V: one 256-coordinate tile, rewritten once the previous tile's P V is done
             const HalfTables tab = make_tables<TV>();
             if (n_tiles > 0)
-                tc_stage<TV, k2Keys>(p.vc, p.seq, p.chunked_v, sm.raw_v[blk], sm.ok[2 + blk], 2 * g + blk, 0, n_keys, key);
+                tc_stage<TV>(p.vc, p.seq, p.chunked_v, sm.raw_v[blk], sm.ok[2 + blk], 2 * g + blk, 0, n_keys, key);
             cp_async_commit();
             for (int i = 0; i < n_tiles; ++i) {
                 cp_async_wait<0>();
+                uint32_t nb[13];
+                tc_window<TV>(sm.raw_v[blk], 2 * g + blk, key, nb);
+                const bool present = sm.ok[2 + blk][key] != 0;
+                if (i + 1 < n_tiles)
+                    tc_stage<TV>(p.vc, p.seq, p.chunked_v, sm.raw_v[blk], sm.ok[2 + blk], 2 * g + blk,
+                                 (int64_t)(i + 1) * k2Keys, n_keys, key);
+                cp_async_commit();
                 if (i >= 1 && !*abort_v &&
                     !tc_wait(bar(k2BarPvFree + ((i - 1) & 1)), (uint32_t)(((i - 1) >> 1) & 1)))
                     *abort_v = 1;
-                tc_decode<TV, true, k2Keys, D>(sm.raw_v[blk], sm.ok[2 + blk], 2 * g + blk, tab, sm.v, nullptr,
-                                               key, kBlock * blk);
+                tc_decode<TV, true, D>(nb, present, tab, sm.v, nullptr, key, kBlock * blk);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_arrive(bar(k2BarVFull));
-                if (i + 1 < n_tiles)
-                    tc_stage<TV, k2Keys>(p.vc, p.seq, p.chunked_v, sm.raw_v[blk], sm.ok[2 + blk], 2 * g + blk,
-                                         (int64_t)(i + 1) * k2Keys, n_keys, key);
-                cp_async_commit();
             }
             cp_async_wait<0>();
         }
