@@ -61,7 +61,7 @@ TRAFFIC = {
     # context), "encode": DRAM bytes of one tq_encode_kv launch of one layer's prefill}
     # Llama-3-8B shape, turbo3: `--kernel-probe 32768` captures of the decode-step and encode
     # kernels under ncu; the encode capture is the benchmark's own launch size.
-    ("llama3-8b-kv-32k", 3): {"attn_per_token": 26493696 / 32768, "encode": 134294528 + 10227968},
+    ("llama3-8b-kv-32k", 3): {"attn_per_token": 26492416 / 32768, "encode": 134294528 + 10227968},
 }
 
 
