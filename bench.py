@@ -593,7 +593,10 @@ def run_ours(args, w, tt, rank, world, local_rank, dist, cpu_baseline_on):
                 "graph_replay_value": world * n_e2e * S * n / (e2e_graph_ms / 1e3),
                 "encode_gbs": world * n_e2e * enc_bytes / (e2e_pre_ms / 1e3) / 1e9,
                 "encode_note": "includes the host-to-device copy of the fp16 prompt rows"},
-        "gpu_launches": K * (L + S * L * 2),
+        # one tq_encode_kv launch per layer; one launch per decode call for a single sequence
+        # (its splits fit one wave and merge inside the launch), two for a batch (attention,
+        # then the merge kernel)
+        "gpu_launches": K * (L + S * L * (1 if n == 1 else 2)),
         "clocks": clk,
         "device_status": status,
         "input_gen_s": t_gen,
