@@ -225,17 +225,20 @@ TQ_API tq_status tq_attn_decode_append(const tq_cache *k, const tq_cache *v,
  * "llama.cpp に TurboQuant を実装" measures in "Numbers on real models"; dequantising
  * inside the Flash-Attention tiles, never forming FP16 K or V in memory, is its roadmap
  * ("Current implementation and what's next").
- *   k, v           caches of one layer; same n_kv_heads; head_dim 128 (other head dims
- *                  return TQ_ERR_UNSUPPORTED); types may differ
+ *   k, v           caches of one layer; same n_kv_heads and head_dim, 128 or 256 (other
+ *                  head dims return TQ_ERR_UNSUPPORTED); types may differ
  *   q_f16          device fp16 [n_q][n_q_heads][head_dim], 16-byte aligned
  *   seq_id         the chunk's sequence; pos0 >= 0 its first position.  The rows of the
  *                  chunk itself must already be in the caches (encode them first).
  *   n_q            queries in the chunk; 0 is a no-op
  *   softmax_scale  score scale; pass 0 for 1/sqrt(head_dim)
  *   out            device fp32 [n_q][n_q_heads][head_dim], 16-byte aligned
+ *   n_q_heads      a multiple of n_kv_heads, at most 128 query heads per KV head
  * No workspace: one CTA per (block of 128 / G query tokens, KV head) covers all the keys
- * its queries see.  Rows the device cannot address (page id or position out of range)
- * are skipped and TQ_ERR_OUT_OF_RANGE is recorded for tq_device_status. */
+ * its queries see, or, at head_dim 128 when that would leave much of the last wave of CTAs
+ * idle, a cluster of two CTAs splits those keys and merges by log-sum-exp in shared
+ * memory.  Rows the device cannot address (page id or position out of range) are skipped
+ * and TQ_ERR_OUT_OF_RANGE is recorded for tq_device_status. */
 TQ_API tq_status tq_attn_prefill(const tq_cache *k, const tq_cache *v, const void *q_f16,
                                  int32_t seq_id, int64_t pos0, int64_t n_q, int n_q_heads,
                                  float softmax_scale, float *out, void *stream);
