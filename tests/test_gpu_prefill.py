@@ -53,6 +53,10 @@ PREFILL_CASES = [
     (2, 2, 1, 8, 500, 33),     # G 8, turbo2, long prefix
     (2, 3, 2, 8, 64, 64),      # mixed types, tile-aligned
     (3, 2, 2, 16, 5, 17),
+    # eight KV heads: the blocks of heads 0..7 start at every even offset mod 16 of a row
+    # (50 g and 34 g bytes), so the producers' 64-byte staging windows see every alignment
+    (2, 2, 8, 16, 129, 40),    # turbo2, G 2
+    (3, 2, 8, 8, 256, 31),     # mixed types, G 1, two full key tiles before the chunk
 ]
 
 
